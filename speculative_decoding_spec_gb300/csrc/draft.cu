@@ -1,0 +1,234 @@
+// draft.cu -- drafter-specific kernels and small pass helpers.
+//
+// The drafter is a light head on the target's last layer: it starts from the
+// target's final hidden state and predicts future tokens autoregressively
+// ("Accelerating Gemini Nano on Pixel with frozen multi-token prediction"
+// (ai-news-spoon), section "The late-exit strategy"), reads the target's KV
+// cache instead of keeping its own (section "Zero-copy architecture"), and
+// scores its output through a clustered shortcut of 2048 centroids ("Gemma 4's
+// MTP drafter explained" (molayo1419.me), section "What is different about
+// Gemma 4's drafter?"; "Gemma 4 acceleration with MTP drafters"
+// (cafe.daangn.com), section "MTP drafter internal optimisations": clustering
+// in the embedder because the final logits are the bottleneck).
+#include <math.h>
+
+#include "common.cuh"
+
+namespace spec {
+
+namespace {
+
+SPEC_DEV float elem(const Mat& W, int K, long long row, int col) {
+  if (W.dtype == DT_F32) return ((const float*)W.data)[row * K + col];
+  if (W.dtype == DT_BF16) return __bfloat162float(((const __nv_bfloat16*)W.data)[row * K + col]);
+  const uint8_t* c = (const uint8_t*)W.data + row * (K / 2);
+  const int b = col >> 5, i = col & 31;
+  const uint8_t byte = c[b * 16 + (i & 15)];
+  const int code = i < 16 ? (byte & 15) : (byte >> 4);
+  return __half2float(((const __half*)W.scales)[row * (K / 32) + b]) * (float)(code - 8);
+}
+
+__global__ void commit_hidden_kernel(int B, const int32_t* seq_ids, const int32_t* sel_row, const float* x,
+                                     int d, const float* g, float eps, float* hid) {
+  __shared__ float red[32];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x;
+  const float* xr = x + (size_t)sel_row[b] * d;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) ss = fmaf(xr[c], xr[c], ss);
+  const float inv = rsqrtf(block_sum(ss, red) / (float)d + eps);
+  float* out = hid + (size_t)seq_ids[b] * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) out[c] = xr[c] * inv * g[c];
+}
+
+__global__ void draft_input_kernel(DraftInArgs a) {
+  __shared__ float red[32];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x, slot = a.seq_ids[b], d = a.d;
+  const float* h = a.h_from_state ? a.h_prev + (size_t)slot * d : a.h_prev + (size_t)b * d;
+  const int tok = a.j == 1 ? a.pending[slot] : a.drafts[b * a.k + a.j - 2];
+  float sh = 0.f, se = 0.f;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    const float e = elem(a.embed, d, tok, c);
+    sh = fmaf(h[c], h[c], sh);
+    se = fmaf(e, e, se);
+  }
+  const float ih = rsqrtf(block_sum(sh, red) / (float)d + a.eps);
+  const float ie = rsqrtf(block_sum(se, red) / (float)d + a.eps);
+  float* cat = a.cat + (size_t)b * 2 * d;
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    cat[c] = h[c] * ih * a.g_h[c];
+    cat[d + c] = elem(a.embed, d, tok, c) * ie * a.g_e[c];
+  }
+  // the drafter's query for step j sits at the position of its input token
+  const int pos = a.seq_len[slot] + a.j - 1;
+  const double lt = log((double)a.theta);
+  for (int j = threadIdx.x; j < a.hd / 2; j += blockDim.x) {
+    double s, c;
+    sincos((double)pos * exp(-2.0 * j / a.hd * lt), &s, &c);
+    a.rope_cs[(size_t)b * a.hd + 2 * j] = (float)c;
+    a.rope_cs[(size_t)b * a.hd + 2 * j + 1] = (float)s;
+  }
+}
+
+// Top-C clusters of one row: bitonic sort of packed (binary32 score, id) keys,
+// larger score first, lower cluster id on ties.
+__global__ void __launch_bounds__(1024) topc_kernel(ClusterArgs a, int cpow2) {
+  extern __shared__ unsigned long long keys[];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x;
+  for (int i = threadIdx.x; i < cpow2; i += blockDim.x)
+    keys[i] = i < a.C ? pack_best(a.scores[(size_t)b * a.C + i], (uint32_t)i) : 0ull;
+  __syncthreads();
+  for (int k = 2; k <= cpow2; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < cpow2; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long x = keys[i], y = keys[ixj];
+          const bool desc = (i & k) == 0;
+          if (desc ? x < y : x > y) {
+            keys[i] = y;
+            keys[ixj] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  for (int r = threadIdx.x; r < a.top_c; r += blockDim.x) a.chosen[b * a.top_c + r] = (int32_t)best_index(keys[r]);
+}
+
+// Score the member rows of one chosen cluster; the best (score, token id) of a
+// row wins with the lower token id on ties. The last CTA writes the draft.
+__global__ void __launch_bounds__(256) members_kernel(ClusterArgs a) {
+  extern __shared__ float ub[];  // normalised drafter state [h]
+  __shared__ float red[32];
+  __shared__ unsigned long long wbest[8];
+  __shared__ int last;
+  grid_dep_wait();
+  grid_dep_launch();
+  const int b = blockIdx.x, ci = blockIdx.y, h = a.h;
+  const float* u = a.u + (size_t)b * h;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < h; c += blockDim.x) ss = fmaf(u[c], u[c], ss);
+  const float inv = rsqrtf(block_sum(ss, red) / (float)h + a.eps);
+  for (int c = threadIdx.x; c < h; c += blockDim.x) ub[c] = u[c] * inv * a.g_out[c];
+  __syncthreads();
+  const int cl = a.chosen[b * a.top_c + ci];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long best = 0ull;
+  for (int r = warp; r < a.cs; r += 8) {
+    const long long p = (long long)cl * a.cs + r;
+    float acc = 0.f;
+    for (int c = lane; c < h; c += 32) acc = fmaf(ub[c], elem(a.vocab, h, p, c), acc);
+    acc = warp_sum(acc);
+    const unsigned long long key = pack_best(acc, (uint32_t)a.perm[p]);
+    best = key > best ? key : best;
+  }
+  if (lane == 0) wbest[warp] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long m = 0ull;
+    for (int w = 0; w < 8; ++w) m = wbest[w] > m ? wbest[w] : m;
+    atomicMax(&a.best[b], m);
+    __threadfence();
+    const unsigned int done = atomicAdd(a.tail.counter, 1u);
+    last = done == gridDim.x * gridDim.y - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int bb = threadIdx.x; bb < a.B; bb += blockDim.x) {
+    const unsigned long long k = volatile_load(a.best + bb);
+    a.tail.draft_out[bb * a.tail.draft_ld + a.tail.draft_j] = (int32_t)best_index(k);
+  }
+  __syncthreads();
+  for (int bb = threadIdx.x; bb < a.B; bb += blockDim.x) a.best[bb] = 0ull;
+  if (threadIdx.x == 0) *a.tail.counter = 0u;
+}
+
+__global__ void inject_kernel(int B, int k, const int32_t* seq_ids, const int32_t* seq_len, int32_t* drafts,
+                              const int32_t* ref, int ref_len, float alpha, const float* draws,
+                              const int32_t* offsets, int vocab, int* err) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int t = threadIdx.x;
+  if (t >= B * k) return;
+  const int b = t / k, j = t % k + 1, slot = seq_ids[b];
+  const int pos = seq_len[slot] + j;
+  if (pos >= ref_len) {
+    set_error(err, SPEC_ERR_REF);
+    return;
+  }
+  const int g = ref[(size_t)slot * ref_len + pos];
+  drafts[t] = draws[t] < alpha ? g : (int32_t)(((long long)g + offsets[t]) % vocab);
+}
+
+cudaLaunchConfig_t cfg_pdl(dim3 grid, dim3 block, size_t smem, cudaStream_t st, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+}  // namespace
+
+int commit_hidden(int B, const int32_t* seq_ids, const int32_t* sel_row, const float* x, int d,
+                  const float* g_final, float eps, float* hid_state, cudaStream_t st) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = cfg_pdl(dim3(B), dim3(256), 0, st, at);
+  return cudaLaunchKernelEx(&cfg, commit_hidden_kernel, B, seq_ids, sel_row, x, d, g_final, eps, hid_state) ==
+                 cudaSuccess ? 1 : -1;
+}
+
+int draft_input(const DraftInArgs& a, cudaStream_t st) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = cfg_pdl(dim3(a.B), dim3(256), 0, st, at);
+  return cudaLaunchKernelEx(&cfg, draft_input_kernel, a) == cudaSuccess ? 1 : -1;
+}
+
+void setup_draft_attributes() {
+  cudaFuncSetAttribute(topc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+}
+
+int cluster_head(const ClusterArgs& a, cudaStream_t st) {
+  int cp = 1;
+  while (cp < a.C) cp <<= 1;
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = cfg_pdl(dim3(a.B), dim3(1024), (size_t)cp * 8, st, at);
+  if (cudaLaunchKernelEx(&cfg, topc_kernel, a, cp) != cudaSuccess) return -1;
+  cudaLaunchConfig_t cfg2 = cfg_pdl(dim3(a.B, a.top_c), dim3(256), (size_t)a.h * 4, st, at);
+  if (cudaLaunchKernelEx(&cfg2, members_kernel, a) != cudaSuccess) return -1;
+  return 2;
+}
+
+int inject_drafts(int B, int k, const int32_t* seq_ids, const int32_t* seq_len, int32_t* drafts,
+                  const int32_t* ref, int ref_len, float alpha, const float* draws, const int32_t* offsets,
+                  int vocab, int* err, cudaStream_t st) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = cfg_pdl(dim3(1), dim3(((B * k + 31) / 32) * 32), 0, st, at);
+  return cudaLaunchKernelEx(&cfg, inject_kernel, B, k, seq_ids, seq_len, drafts, ref, ref_len, alpha, draws,
+                            offsets, vocab, err) == cudaSuccess ? 1 : -1;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+}  // namespace spec

@@ -1,0 +1,179 @@
+// kernels.h -- internal interface between the C-ABI controller and the
+// sm_103a kernels. Plain types only; every launcher enqueues on `st` and
+// returns the number of kernels it launched (negative on a launch error).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace spec {
+
+enum { DT_F32 = 0, DT_BF16 = 1, DT_Q4_0 = 2 };
+
+// Device error word values (first error wins).
+enum { SPEC_ERR_NONE = 0, SPEC_ERR_TOKEN = 1, SPEC_ERR_CAPACITY = 2, SPEC_ERR_REF = 3 };
+
+// One row-major matrix [N][K] (a layer of a stack, offset already applied).
+struct Mat {
+  int dtype;
+  const void* data;
+  const void* scales;  // Q4_0 only: fp16 [N][K/32]
+};
+
+// Byte offset of layer l of a stack of [N][K] matrices.
+inline Mat mat_layer(Mat m, int l, int N, int K) {
+  long long e = (long long)l * N * K;
+  if (m.dtype == DT_F32) m.data = (const char*)m.data + e * 4;
+  else if (m.dtype == DT_BF16) m.data = (const char*)m.data + e * 2;
+  else {
+    m.data = (const char*)m.data + e / 2;
+    m.scales = (const char*)m.scales + (e / 32) * 2;
+  }
+  return m;
+}
+
+enum Epi { EPI_STORE = 0, EPI_ADD = 1, EPI_GEGLU = 2, EPI_ARGMAX = 3 };
+enum Tail { TAIL_NONE = 0, TAIL_VERIFY = 1, TAIL_PREFILL = 2, TAIL_DRAFT = 3 };
+
+// What the last CTA of an argmax launch does once every row's argmax is known.
+struct TailArgs {
+  int mode;
+  int B, R, k;
+  const int32_t* seq_ids;   // [B]
+  const int32_t* drafts;    // VERIFY: [B][k]
+  int32_t* out_tokens;      // VERIFY: [B][k+1]
+  int32_t* n_emitted;       // VERIFY: [B]
+  int32_t* seq_len;         // state [slots]
+  int32_t* pending;         // state [slots]
+  int64_t* stats;           // state [slots][4]
+  int32_t* sel_row;         // [B] pass row whose hidden seeds the drafter
+  int32_t* draft_out;       // DRAFT: [B][draft_ld]
+  int draft_ld, draft_j;
+  const int32_t* token_of;  // optional row -> token id map (clustered head)
+  unsigned long long* best_all;  // every pass row's packed argmax, zeroed by the last CTA
+  unsigned int* counter;    // arrival counter, reset by the last CTA
+  int* err;
+};
+
+struct GemvArgs {
+  const float* X;           // [M][ldx] fp32 activations
+  int ldx, M, N, K;
+  Mat W;
+  const float* gain;        // RMSNorm prologue gain [K] (nullptr: none)
+  float eps;
+  int epi;
+  float* Y;                 // output [M][ldy] (STORE / ADD / GEGLU; ARGMAX: optional logits)
+  int ldy;
+  int geglu_half;           // GEGLU: rows j and j+half pair; Y has `half` columns
+  unsigned long long* best; // ARGMAX: [M] packed (score, row) keys, zero before the launch
+  TailArgs tail;
+  int pdl;                  // launch with programmatic dependent launch
+};
+int gemv(const GemvArgs& a, cudaStream_t st);
+
+// Per-pass row setup: tokens, positions and RoPE cos/sin for M = B*R rows.
+struct RowsArgs {
+  int B, R, mode;           // mode: TAIL_VERIFY (rows = [pending, drafts]) or TAIL_PREFILL
+  const int32_t* seq_ids;
+  const int32_t* tokens;    // PREFILL: [B][R]; VERIFY: drafts [B][R-1]
+  const int32_t* pending;
+  const int32_t* seq_len;
+  Mat embed;
+  int d, hd;
+  float theta;
+  float* x;                 // [M][d] embedding rows (fp32)
+  int32_t* pos;             // [M]
+  float* rope_cs;           // [M][hd/2][2]
+  int* err;
+  int vocab;
+};
+int embed_rows(const RowsArgs& a, cudaStream_t st);
+
+struct RopeAppendArgs {
+  float* qkv;               // [M][nqkv] in/out: q and k rotated in place
+  int M, R, nq, nkv, hd;
+  const float* rope_cs;
+  const int32_t* pos;       // [M]
+  const int32_t* seq_ids;
+  void* pool;
+  int kv_dtype;
+  long long layer_elems;    // elements per layer of the pool
+  int layer, n_pages, max_pages;
+  const int32_t* block_table;
+  int* err;
+};
+int rope_append(const RopeAppendArgs& a, cudaStream_t st);
+
+struct AttnArgs {
+  const float* q;           // [M][ldq]; head h at column h*hd
+  int ldq;
+  int B, R, nq, nkv, hd;
+  int key_extra;            // keys of row i: [0, seq_len + i + key_extra)
+  const void* pool;
+  int kv_dtype;
+  long long layer_elems;
+  int layer, n_pages, max_pages;
+  const int32_t* block_table;
+  const int32_t* seq_ids;
+  const int32_t* seq_len;
+  const float* rope_cs;     // when non-null, q is rotated on load with [M][hd/2][2]
+  int n_split, pages_per_split;
+  float* part_o;            // [M][nq][n_split][hd]
+  float* part_ml;           // [M][nq][n_split][2]
+  float* out;               // [M][nq*hd] merged output
+  int* err;
+};
+int attention(const AttnArgs& a, cudaStream_t st);
+
+// Final-normed hidden state of the row chosen by the accept step -> slot state.
+int commit_hidden(int B, const int32_t* seq_ids, const int32_t* sel_row, const float* x, int d,
+                  const float* g_final, float eps, float* hid_state, cudaStream_t st);
+
+// Drafter step input: cat[b] = [N(h); N(E[tok])], RoPE table at the draft position.
+struct DraftInArgs {
+  int B, j, k, d, hd;
+  const int32_t* seq_ids;
+  const float* h_prev;      // j == 1: slot state hid[slot]; else [B][d]
+  int h_from_state;
+  const int32_t* pending;
+  const int32_t* drafts;    // [B][k] (token of step j-1 when j > 1)
+  const int32_t* seq_len;
+  Mat embed;
+  const float* g_h;
+  const float* g_e;
+  float eps, theta;
+  float* cat;               // [B][2d]
+  float* rope_cs;           // [B][hd/2][2]
+};
+int draft_input(const DraftInArgs& a, cudaStream_t st);
+
+// Clustered head: top-C clusters per row, then member scoring + argmax.
+struct ClusterArgs {
+  int B, C, top_c, cs, h;
+  const float* scores;      // [B][C] centroid scores
+  int32_t* chosen;          // [B][top_c]
+  const float* u;           // [B][h] raw drafter state (normalised here)
+  const float* g_out;
+  float eps;
+  Mat vocab;                // [V][h] cluster-sorted rows
+  const int32_t* perm;
+  unsigned long long* best; // [B]
+  TailArgs tail;
+};
+int cluster_head(const ClusterArgs& a, cudaStream_t st);
+
+int inject_drafts(int B, int k, const int32_t* seq_ids, const int32_t* seq_len, int32_t* drafts,
+                  const int32_t* ref, int ref_len, float alpha, const float* draws,
+                  const int32_t* offsets, int vocab, int* err, cudaStream_t st);
+
+// Set the dynamic shared-memory limits of every kernel (call once, outside
+// stream capture).
+void setup_gemv_attributes();
+void setup_gemv_tc_attributes();
+int gemv_tc(const GemvArgs& a, cudaStream_t st);
+void setup_attn_attributes();
+void setup_draft_attributes();
+
+int num_sms();
+size_t attention_smem(int hd, int qn);
+
+}  // namespace spec

@@ -1,0 +1,560 @@
+// spec_api.cu -- the C ABI (include/spec.h): host-side validation, workspace
+// layout, the draft / verify / accept pass as a kernel sequence on one stream,
+// and a cache of CUDA graphs keyed by call shape.
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/spec.h"
+#include "kernels.h"
+
+using namespace spec;
+
+namespace {
+
+struct Buf {
+  size_t off = 0;
+  template <typename T>
+  T* take(char* base, size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+struct Work {
+  // target pass
+  float *x, *qkv, *att, *act, *part_o, *part_ml, *rope_cs;
+  int32_t *pos, *sel_row, *n_emit1;
+  unsigned long long* best;
+  unsigned int* counter;
+  int* err;
+  // drafter
+  float *d_cat, *d_u, *d_q, *d_att, *d_act, *d_h, *d_scores, *d_rope, *d_part_o, *d_part_ml;
+  int32_t *d_chosen, *d_drafts;
+  unsigned long long* d_best;
+  unsigned int* d_counter;
+  size_t bytes;
+};
+
+constexpr int KMAX = 16;
+
+Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int B_max, int rows_max,
+           int max_pages) {
+  Work w = {};
+  Buf b;
+  const size_t M = (size_t)B_max * rows_max;
+  const int nqkv = (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim, qd = m.n_q_heads * m.head_dim;
+  w.x = b.take<float>(base, M * m.d_model);
+  w.qkv = b.take<float>(base, M * nqkv);
+  w.att = b.take<float>(base, M * qd);
+  w.act = b.take<float>(base, M * m.d_ff);
+  w.part_o = b.take<float>(base, M * m.n_q_heads * (size_t)max_pages * m.head_dim);
+  w.part_ml = b.take<float>(base, M * m.n_q_heads * (size_t)max_pages * 2);
+  w.rope_cs = b.take<float>(base, M * m.head_dim);
+  w.pos = b.take<int32_t>(base, M);
+  w.sel_row = b.take<int32_t>(base, B_max);
+  w.n_emit1 = b.take<int32_t>(base, B_max);
+  w.best = b.take<unsigned long long>(base, M);
+  w.counter = b.take<unsigned int>(base, 4);
+  w.err = b.take<int>(base, 4);
+  if (d) {
+    const int dq = d->n_q_heads * m.head_dim;
+    w.d_cat = b.take<float>(base, (size_t)B_max * 2 * m.d_model);
+    w.d_u = b.take<float>(base, (size_t)B_max * d->hidden);
+    w.d_q = b.take<float>(base, (size_t)B_max * dq);
+    w.d_att = b.take<float>(base, (size_t)B_max * dq);
+    w.d_act = b.take<float>(base, (size_t)B_max * d->d_ff);
+    w.d_h = b.take<float>(base, (size_t)B_max * m.d_model);
+    w.d_scores = b.take<float>(base, (size_t)B_max * std::max(d->n_centroids, 1));
+    w.d_rope = b.take<float>(base, (size_t)B_max * m.head_dim);
+    w.d_part_o = b.take<float>(base, (size_t)B_max * d->n_q_heads * max_pages * m.head_dim);
+    w.d_part_ml = b.take<float>(base, (size_t)B_max * d->n_q_heads * max_pages * 2);
+    w.d_chosen = b.take<int32_t>(base, (size_t)B_max * std::max(d->top_c, 1));
+    w.d_drafts = b.take<int32_t>(base, (size_t)B_max * KMAX);
+    w.d_best = b.take<unsigned long long>(base, B_max);
+    w.d_counter = b.take<unsigned int>(base, 4);
+  }
+  w.bytes = (b.off + 255) & ~size_t(255);
+  return w;
+}
+
+bool mat_ok(const spec_matrix& mm, int K) {
+  if (!mm.data) return false;
+  if (mm.dtype == SPEC_Q4_0) return mm.scales && K % 32 == 0;
+  if (mm.dtype == SPEC_F32 || mm.dtype == SPEC_BF16) return K % 8 == 0;
+  return false;
+}
+
+Mat M_(const spec_matrix& m) { return Mat{m.dtype, m.data, m.scales}; }
+
+bool model_ok(const spec_model_desc& m) {
+  return m.n_layers > 0 && m.d_model > 0 && m.n_q_heads > 0 && m.n_kv_heads > 0 && m.head_dim > 0 &&
+         m.head_dim % 2 == 0 && m.head_dim <= 256 && m.n_q_heads % m.n_kv_heads == 0 && m.d_ff > 0 &&
+         m.vocab > 1 && (m.kv_dtype == SPEC_F32 || m.kv_dtype == SPEC_BF16) && m.d_model % 8 == 0 &&
+         m.d_ff % 8 == 0 && (m.w_dtype != SPEC_Q4_0 || (m.d_model % 32 == 0 && m.d_ff % 32 == 0 &&
+                                                     (m.n_q_heads * m.head_dim) % 32 == 0));
+}
+
+bool drafter_ok(const spec_model_desc& m, const spec_drafter_desc& d) {
+  if (d.n_layers <= 0 || d.hidden <= 0 || d.d_ff <= 0 || d.n_q_heads <= 0) return false;
+  if (d.n_q_heads % m.n_kv_heads) return false;
+  if (d.hidden % 8 || d.d_ff % 8) return false;
+  if (d.w_dtype == SPEC_Q4_0 && (d.hidden % 32 || d.d_ff % 32)) return false;
+  if (d.clustered) {
+    if (d.n_centroids <= 0 || d.n_centroids > 8192 || m.vocab % d.n_centroids) return false;
+    if (d.top_c <= 0 || d.top_c > d.n_centroids) return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+struct spec_ctx {
+  spec_model_desc m;
+  spec_weights w;
+  bool has_drafter = false;
+  spec_drafter_desc dd;
+  spec_drafter_weights dw;
+  spec_kv_desc kv;
+  spec_state state;
+  int B_max, rows_max;
+  long long layer_elems;
+  Work wk;
+  bool graphs = true;
+  long long launches = 0;
+  struct Entry {
+    cudaGraphExec_t exec;
+    int kernels;
+  };
+  std::map<std::string, Entry> cache;
+  std::mutex mu;
+};
+
+namespace {
+
+int kv_dt(const spec_ctx* c) { return c->m.kv_dtype == SPEC_F32 ? DT_F32 : DT_BF16; }
+
+// ---- the target pass: rows -> layers -> LM head + argmax + accept -----------
+int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, const int32_t* tokens,
+                 int32_t* out_tokens, int32_t* n_emitted, float* logits, cudaStream_t st) {
+  const spec_model_desc& m = c->m;
+  const Work& w = c->wk;
+  const int M = B * R, d = m.d_model, hd = m.head_dim, nq = m.n_q_heads, nkv = m.n_kv_heads;
+  const int nqkv = (nq + 2 * nkv) * hd, qd = nq * hd, ff = m.d_ff;
+  int n = 0, r;
+#define LAUNCH(expr)        \
+  do {                      \
+    r = (expr);             \
+    if (r < 0) return -1;   \
+    n += r;                 \
+  } while (0)
+
+  RowsArgs ra = {};
+  ra.B = B; ra.R = R; ra.mode = mode; ra.seq_ids = seq_ids; ra.tokens = tokens;
+  ra.pending = c->state.pending; ra.seq_len = c->state.seq_len; ra.embed = M_(c->w.embed);
+  ra.d = d; ra.hd = hd; ra.theta = m.rope_theta; ra.x = w.x; ra.pos = w.pos; ra.rope_cs = w.rope_cs;
+  ra.err = w.err; ra.vocab = m.vocab;
+  LAUNCH(embed_rows(ra, st));
+
+  for (int l = 0; l < m.n_layers; ++l) {
+    GemvArgs g = {};
+    g.X = w.x; g.ldx = d; g.M = M; g.N = nqkv; g.K = d;
+    g.W = mat_layer(M_(c->w.wqkv), l, nqkv, d);
+    g.gain = c->w.g_attn + (size_t)l * d; g.eps = m.rms_eps;
+    g.epi = EPI_STORE; g.Y = w.qkv; g.ldy = nqkv; g.pdl = 1;
+    LAUNCH(gemv(g, st));
+
+    RopeAppendArgs rp = {};
+    rp.qkv = w.qkv; rp.M = M; rp.R = R; rp.nq = nq; rp.nkv = nkv; rp.hd = hd; rp.rope_cs = w.rope_cs;
+    rp.pos = w.pos; rp.seq_ids = seq_ids; rp.pool = c->kv.pool; rp.kv_dtype = kv_dt(c);
+    rp.layer_elems = c->layer_elems; rp.layer = l; rp.n_pages = c->kv.n_pages;
+    rp.max_pages = c->kv.max_pages_per_seq; rp.block_table = c->kv.block_table; rp.err = w.err;
+    LAUNCH(rope_append(rp, st));
+
+    AttnArgs at = {};
+    at.q = w.qkv; at.ldq = nqkv; at.B = B; at.R = R; at.nq = nq; at.nkv = nkv; at.hd = hd;
+    at.key_extra = 1; at.pool = c->kv.pool; at.kv_dtype = kv_dt(c); at.layer_elems = c->layer_elems;
+    at.layer = l; at.n_pages = c->kv.n_pages; at.max_pages = c->kv.max_pages_per_seq;
+    at.block_table = c->kv.block_table; at.seq_ids = seq_ids; at.seq_len = c->state.seq_len;
+    at.rope_cs = nullptr; at.n_split = c->kv.max_pages_per_seq; at.pages_per_split = 1;
+    at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.att; at.err = w.err;
+    LAUNCH(attention(at, st));
+
+    g = GemvArgs{};
+    g.X = w.att; g.ldx = qd; g.M = M; g.N = d; g.K = qd;
+    g.W = mat_layer(M_(c->w.wo), l, d, qd);
+    g.epi = EPI_ADD; g.Y = w.x; g.ldy = d; g.pdl = 1;
+    LAUNCH(gemv(g, st));
+
+    g = GemvArgs{};
+    g.X = w.x; g.ldx = d; g.M = M; g.N = 2 * ff; g.K = d;
+    g.W = mat_layer(M_(c->w.wgu), l, 2 * ff, d);
+    g.gain = c->w.g_ffn + (size_t)l * d; g.eps = m.rms_eps;
+    g.epi = EPI_GEGLU; g.geglu_half = ff; g.Y = w.act; g.ldy = ff; g.pdl = 1;
+    LAUNCH(gemv(g, st));
+
+    g = GemvArgs{};
+    g.X = w.act; g.ldx = ff; g.M = M; g.N = d; g.K = ff;
+    g.W = mat_layer(M_(c->w.wdown), l, d, ff);
+    g.epi = EPI_ADD; g.Y = w.x; g.ldy = d; g.pdl = 1;
+    LAUNCH(gemv(g, st));
+  }
+
+  GemvArgs g = {};
+  g.X = w.x; g.ldx = d; g.M = M; g.N = m.vocab; g.K = d;
+  g.W = M_(c->w.embed);
+  g.gain = c->w.g_final; g.eps = m.rms_eps;
+  g.epi = EPI_ARGMAX; g.Y = logits; g.ldy = m.vocab; g.best = w.best; g.pdl = 1;
+  TailArgs& t = g.tail;
+  t.mode = mode; t.B = B; t.R = R; t.k = R - 1; t.seq_ids = seq_ids; t.drafts = tokens;
+  t.out_tokens = out_tokens; t.n_emitted = n_emitted; t.seq_len = c->state.seq_len;
+  t.pending = c->state.pending; t.stats = c->state.stats; t.sel_row = w.sel_row;
+  t.best_all = w.best; t.counter = w.counter; t.err = w.err;
+  LAUNCH(gemv(g, st));
+  LAUNCH(commit_hidden(B, seq_ids, w.sel_row, w.x, d, c->w.g_final, m.rms_eps, c->state.hid, st));
+  return n;
+}
+
+// ---- the drafter: k autoregressive steps on the target's last hidden state ---
+int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* drafts, cudaStream_t st) {
+  const spec_model_desc& m = c->m;
+  const spec_drafter_desc& dd = c->dd;
+  const spec_drafter_weights& dw = c->dw;
+  const Work& w = c->wk;
+  const int d = m.d_model, h = dd.hidden, hd = m.head_dim, dq = dd.n_q_heads * hd, ff = dd.d_ff;
+  int n = 0, r;
+  for (int j = 1; j <= k; ++j) {
+    DraftInArgs di = {};
+    di.B = B; di.j = j; di.k = k; di.d = d; di.hd = hd; di.seq_ids = seq_ids;
+    di.h_prev = j == 1 ? c->state.hid : w.d_h; di.h_from_state = j == 1;
+    di.pending = c->state.pending; di.drafts = drafts; di.seq_len = c->state.seq_len;
+    di.embed = M_(c->w.embed); di.g_h = dw.g_in_h; di.g_e = dw.g_in_e; di.eps = m.rms_eps;
+    di.theta = m.rope_theta; di.cat = w.d_cat; di.rope_cs = w.d_rope;
+    LAUNCH(draft_input(di, st));
+
+    GemvArgs g = {};
+    g.X = w.d_cat; g.ldx = 2 * d; g.M = B; g.N = h; g.K = 2 * d; g.W = M_(dw.w_in);
+    g.epi = EPI_STORE; g.Y = w.d_u; g.ldy = h; g.pdl = 1;
+    LAUNCH(gemv(g, st));
+
+    for (int l = 0; l < dd.n_layers; ++l) {
+      g = GemvArgs{};
+      g.X = w.d_u; g.ldx = h; g.M = B; g.N = dq; g.K = h; g.W = mat_layer(M_(dw.wq), l, dq, h);
+      g.gain = dw.g_attn + (size_t)l * h; g.eps = m.rms_eps;
+      g.epi = EPI_STORE; g.Y = w.d_q; g.ldy = dq; g.pdl = 1;
+      LAUNCH(gemv(g, st));
+
+      AttnArgs at = {};
+      at.q = w.d_q; at.ldq = dq; at.B = B; at.R = 1; at.nq = dd.n_q_heads; at.nkv = m.n_kv_heads;
+      at.hd = hd; at.key_extra = 0; at.pool = c->kv.pool; at.kv_dtype = kv_dt(c);
+      at.layer_elems = c->layer_elems; at.layer = m.n_layers - 1; at.n_pages = c->kv.n_pages;
+      at.max_pages = c->kv.max_pages_per_seq; at.block_table = c->kv.block_table; at.seq_ids = seq_ids;
+      at.seq_len = c->state.seq_len; at.rope_cs = w.d_rope; at.n_split = c->kv.max_pages_per_seq;
+      at.pages_per_split = 1; at.part_o = w.d_part_o; at.part_ml = w.d_part_ml; at.out = w.d_att;
+      at.err = w.err;
+      LAUNCH(attention(at, st));
+
+      g = GemvArgs{};
+      g.X = w.d_att; g.ldx = dq; g.M = B; g.N = h; g.K = dq; g.W = mat_layer(M_(dw.wo), l, h, dq);
+      g.epi = EPI_ADD; g.Y = w.d_u; g.ldy = h; g.pdl = 1;
+      LAUNCH(gemv(g, st));
+
+      g = GemvArgs{};
+      g.X = w.d_u; g.ldx = h; g.M = B; g.N = 2 * ff; g.K = h; g.W = mat_layer(M_(dw.wgu), l, 2 * ff, h);
+      g.gain = dw.g_ffn + (size_t)l * h; g.eps = m.rms_eps;
+      g.epi = EPI_GEGLU; g.geglu_half = ff; g.Y = w.d_act; g.ldy = ff; g.pdl = 1;
+      LAUNCH(gemv(g, st));
+
+      g = GemvArgs{};
+      g.X = w.d_act; g.ldx = ff; g.M = B; g.N = h; g.K = ff; g.W = mat_layer(M_(dw.wdown), l, h, ff);
+      g.epi = EPI_ADD; g.Y = w.d_u; g.ldy = h; g.pdl = 1;
+      LAUNCH(gemv(g, st));
+    }
+
+    // next hidden state h_j = W_out . u
+    g = GemvArgs{};
+    g.X = w.d_u; g.ldx = h; g.M = B; g.N = d; g.K = h; g.W = M_(dw.w_out);
+    g.epi = EPI_STORE; g.Y = w.d_h; g.ldy = d; g.pdl = 1;
+    LAUNCH(gemv(g, st));
+
+    if (!dd.clustered) {
+      g = GemvArgs{};
+      g.X = w.d_u; g.ldx = h; g.M = B; g.N = m.vocab; g.K = h; g.W = M_(dw.vocab);
+      g.gain = dw.g_out; g.eps = m.rms_eps; g.epi = EPI_ARGMAX; g.best = w.d_best; g.pdl = 1;
+      TailArgs& t = g.tail;
+      t.mode = TAIL_DRAFT; t.B = B; t.R = 1; t.k = k; t.seq_ids = seq_ids; t.draft_out = drafts;
+      t.draft_ld = k; t.draft_j = j - 1; t.best_all = w.d_best; t.counter = w.d_counter; t.err = w.err;
+      LAUNCH(gemv(g, st));
+    } else {
+      g = GemvArgs{};
+      g.X = w.d_u; g.ldx = h; g.M = B; g.N = dd.n_centroids; g.K = h; g.W = M_(dw.centroids);
+      g.gain = dw.g_out; g.eps = m.rms_eps; g.epi = EPI_STORE; g.Y = w.d_scores; g.ldy = dd.n_centroids;
+      g.pdl = 1;
+      LAUNCH(gemv(g, st));
+      ClusterArgs ca = {};
+      ca.B = B; ca.C = dd.n_centroids; ca.top_c = dd.top_c; ca.cs = m.vocab / dd.n_centroids; ca.h = h;
+      ca.scores = w.d_scores; ca.chosen = w.d_chosen; ca.u = w.d_u; ca.g_out = dw.g_out; ca.eps = m.rms_eps;
+      ca.vocab = M_(dw.vocab); ca.perm = dw.perm; ca.best = w.d_best;
+      ca.tail.mode = TAIL_DRAFT; ca.tail.B = B; ca.tail.draft_out = drafts; ca.tail.draft_ld = k;
+      ca.tail.draft_j = j - 1; ca.tail.counter = w.d_counter;
+      LAUNCH(cluster_head(ca, st));
+    }
+  }
+  return n;
+#undef LAUNCH
+}
+
+// Run `fn` eagerly, or through a cached CUDA graph keyed by `key`.
+template <typename F>
+spec_status run_graph(spec_ctx* c, const std::string& key, cudaStream_t st, F fn) {
+  if (!c->graphs || st == nullptr) {
+    const int n = fn(st);
+    if (n < 0) return SPEC_ECUDA;
+    c->launches += n;
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+  }
+  std::lock_guard<std::mutex> lk(c->mu);
+  auto it = c->cache.find(key);
+  if (it == c->cache.end()) {
+    cudaGraph_t graph;
+    if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return SPEC_ECUDA;
+    const int n = fn(st);
+    const cudaError_t e = cudaStreamEndCapture(st, &graph);
+    if (n < 0 || e != cudaSuccess) {
+      if (e == cudaSuccess) cudaGraphDestroy(graph);
+      cudaGetLastError();
+      return SPEC_ECUDA;
+    }
+    cudaGraphExec_t exec;
+    const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ie != cudaSuccess) return SPEC_ECUDA;
+    it = c->cache.emplace(key, spec_ctx::Entry{exec, n}).first;
+  }
+  if (cudaGraphLaunch(it->second.exec, st) != cudaSuccess) return SPEC_ECUDA;
+  c->launches += it->second.kernels;
+  return SPEC_OK;
+}
+
+std::string key_of(const char* op, std::initializer_list<long long> v) {
+  std::string s(op);
+  char buf[32];
+  for (long long x : v) {
+    snprintf(buf, sizeof buf, ":%llx", x);
+    s += buf;
+  }
+  return s;
+}
+
+bool batch_ok(const spec_ctx* c, int B, const int32_t* seq_ids) {
+  return c && B > 0 && B <= c->B_max && seq_ids;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_workspace_bytes(const spec_model_desc* m, const spec_drafter_desc* d, int32_t B_max, int32_t rows_max,
+                            int32_t max_pages_per_seq) {
+  if (!m || !model_ok(*m) || B_max <= 0 || rows_max <= 0 || max_pages_per_seq <= 0) return 0;
+  if (d && !drafter_ok(*m, *d)) return 0;
+  return carve(nullptr, *m, d, B_max, rows_max, max_pages_per_seq).bytes;
+}
+
+spec_status spec_init(const spec_model_desc* model, const spec_weights* weights, const spec_drafter_desc* drafter,
+                      const spec_drafter_weights* dweights, const spec_kv_desc* kv, const spec_state* state,
+                      int32_t B_max, int32_t rows_max, void* workspace, size_t ws_bytes, void* stream,
+                      spec_ctx** out) {
+  if (!out || !model || !weights || !kv || !state || !workspace) return SPEC_EINVAL;
+  *out = nullptr;
+  const spec_model_desc& m = *model;
+  if (!model_ok(m)) return SPEC_EINVAL;
+  if (B_max <= 0 || rows_max <= 0 || rows_max > 64) return SPEC_EINVAL;
+  if (kv->page_size != 64 || !kv->pool || !kv->block_table || kv->n_pages <= 0 || kv->max_pages_per_seq <= 0 ||
+      kv->n_slots < B_max)
+    return SPEC_EINVAL;
+  if (!state->seq_len || !state->pending || !state->hid || !state->stats) return SPEC_EINVAL;
+  const int nqkv = (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim, qd = m.n_q_heads * m.head_dim;
+  const spec_weights& w = *weights;
+  if (!mat_ok(w.embed, m.d_model) || !mat_ok(w.wqkv, m.d_model) || !mat_ok(w.wo, qd) ||
+      !mat_ok(w.wgu, m.d_model) || !mat_ok(w.wdown, m.d_ff) || !w.g_attn || !w.g_ffn || !w.g_final)
+    return SPEC_EINVAL;
+  for (const spec_matrix* mm : {&w.embed, &w.wqkv, &w.wo, &w.wgu, &w.wdown})
+    if (mm->dtype != m.w_dtype) return SPEC_EINVAL;
+  (void)nqkv;
+  const int G = m.n_q_heads / m.n_kv_heads;
+  if (attention_smem(m.head_dim, rows_max * G) > 200 * 1024) return SPEC_EUNSUPPORTED;
+  if (drafter) {
+    if (!dweights || !drafter_ok(m, *drafter)) return SPEC_EINVAL;
+    const spec_drafter_weights& dw = *dweights;
+    const int h = drafter->hidden, dq = drafter->n_q_heads * m.head_dim;
+    if (!mat_ok(dw.w_in, 2 * m.d_model) || !mat_ok(dw.wq, h) || !mat_ok(dw.wo, dq) || !mat_ok(dw.wgu, h) ||
+        !mat_ok(dw.wdown, drafter->d_ff) || !mat_ok(dw.w_out, h) || !mat_ok(dw.vocab, h) || !dw.g_in_h ||
+        !dw.g_in_e || !dw.g_attn || !dw.g_ffn || !dw.g_out)
+      return SPEC_EINVAL;
+    if (drafter->clustered && (!mat_ok(dw.centroids, h) || !dw.perm)) return SPEC_EINVAL;
+    if (attention_smem(m.head_dim, drafter->n_q_heads / m.n_kv_heads) > 200 * 1024) return SPEC_EUNSUPPORTED;
+  }
+  const Work need = carve(nullptr, m, drafter, B_max, rows_max, kv->max_pages_per_seq);
+  if (ws_bytes < need.bytes) return SPEC_ECAPACITY;
+
+  spec_ctx* c = new spec_ctx();
+  c->m = m;
+  c->w = w;
+  c->has_drafter = drafter != nullptr;
+  if (drafter) {
+    c->dd = *drafter;
+    c->dw = *dweights;
+  }
+  c->kv = *kv;
+  c->state = *state;
+  c->B_max = B_max;
+  c->rows_max = rows_max;
+  c->layer_elems = (long long)kv->n_pages * 2 * m.n_kv_heads * 64 * m.head_dim;
+  c->wk = carve((char*)workspace, m, drafter, B_max, rows_max, kv->max_pages_per_seq);
+  setup_gemv_attributes();
+  setup_attn_attributes();
+  setup_draft_attributes();
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(workspace, 0, need.bytes, st) != cudaSuccess) {
+    delete c;
+    return SPEC_ECUDA;
+  }
+  *out = c;
+  return SPEC_OK;
+}
+
+spec_status spec_prefill(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t R, const int32_t* tokens,
+                         void* stream) {
+  if (!batch_ok(c, B, seq_ids) || R <= 0 || R > c->rows_max || !tokens) return SPEC_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  return run_graph(c, key_of("prefill", {B, R, (long long)seq_ids, (long long)tokens, (long long)st}), st,
+                   [&](cudaStream_t s) {
+                     return enqueue_pass(c, B, seq_ids, R, TAIL_PREFILL, tokens, nullptr, nullptr, nullptr, s);
+                   });
+}
+
+spec_status spec_verify(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t k, const int32_t* drafts,
+                        int32_t* out_tokens, int32_t* n_emitted, float* logits_dbg, void* stream) {
+  if (!batch_ok(c, B, seq_ids) || k < 0 || k > KMAX || k + 1 > c->rows_max || !out_tokens || !n_emitted ||
+      (k > 0 && !drafts))
+    return SPEC_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  return run_graph(c,
+                   key_of("verify", {B, k, (long long)seq_ids, (long long)drafts, (long long)out_tokens,
+                                     (long long)n_emitted, (long long)logits_dbg, (long long)st}),
+                   st, [&](cudaStream_t s) {
+                     return enqueue_pass(c, B, seq_ids, k + 1, TAIL_VERIFY, drafts, out_tokens, n_emitted,
+                                         logits_dbg, s);
+                   });
+}
+
+spec_status spec_draft(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t k, int32_t* drafts, void* stream) {
+  if (!batch_ok(c, B, seq_ids) || k <= 0 || k > KMAX || !drafts) return SPEC_EINVAL;
+  if (!c->has_drafter) return SPEC_ESTATE;
+  cudaStream_t st = (cudaStream_t)stream;
+  return run_graph(c, key_of("draft", {B, k, (long long)seq_ids, (long long)drafts, (long long)st}), st,
+                   [&](cudaStream_t s) { return enqueue_draft(c, B, seq_ids, k, drafts, s); });
+}
+
+spec_status spec_step(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t k, int32_t* out_tokens,
+                      int32_t* n_emitted, void* stream) {
+  if (!batch_ok(c, B, seq_ids)) return SPEC_EINVAL;
+  spec_status s = spec_draft(c, B, seq_ids, k, c->wk.d_drafts, stream);
+  if (s != SPEC_OK) return s;
+  return spec_verify(c, B, seq_ids, k, c->wk.d_drafts, out_tokens, n_emitted, nullptr, stream);
+}
+
+spec_status spec_decode(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t* out_tok, void* stream) {
+  if (!batch_ok(c, B, seq_ids) || !out_tok) return SPEC_EINVAL;
+  // n_emitted is always 1 for k = 0; it lands in a workspace buffer
+  return spec_verify(c, B, seq_ids, 0, nullptr, out_tok, c->wk.n_emit1, nullptr, stream);
+}
+
+spec_status spec_inject_drafts(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t k, int32_t* drafts,
+                               const int32_t* ref, int32_t ref_len, float alpha, const float* draws,
+                               const int32_t* offsets, void* stream) {
+  if (!batch_ok(c, B, seq_ids) || k <= 0 || k > KMAX || !drafts || !ref || ref_len <= 0 || !draws || !offsets)
+    return SPEC_EINVAL;
+  const int n = inject_drafts(B, k, seq_ids, c->state.seq_len, drafts, ref, ref_len, alpha, draws, offsets,
+                              c->m.vocab, c->wk.err, (cudaStream_t)stream);
+  if (n < 0) return SPEC_ECUDA;
+  c->launches += n;
+  return SPEC_OK;
+}
+
+spec_status spec_linear(const spec_matrix* w, int32_t N, int32_t K, const float* x, int32_t M, const float* gain,
+                        float eps, float* y, void* stream) {
+  if (!w || !x || !y || N <= 0 || K <= 0 || M <= 0 || M > 64 || !mat_ok(*w, K)) return SPEC_EINVAL;
+  GemvArgs g = {};
+  g.X = x; g.ldx = K; g.M = M; g.N = N; g.K = K; g.W = M_(*w); g.gain = gain; g.eps = eps;
+  g.epi = EPI_STORE; g.Y = y; g.ldy = N; g.pdl = 0;
+  static std::once_flag once;
+  std::call_once(once, setup_gemv_attributes);
+  if (gemv(g, (cudaStream_t)stream) < 0) return SPEC_ECUDA;
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+spec_status spec_stats(spec_ctx* c, int32_t slot, spec_stats_t* out, void* stream) {
+  if (!c || !out || slot < 0 || slot >= c->kv.n_slots) return SPEC_EINVAL;
+  int64_t v[4];
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(v, c->state.stats + (size_t)slot * 4, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return SPEC_ECUDA;
+  out->passes = v[0];
+  out->drafted = v[1];
+  out->accepted = v[2];
+  out->emitted = v[3];
+  out->tokens_per_pass = v[0] ? (double)v[3] / (double)v[0] : 0.0;
+  return SPEC_OK;
+}
+
+spec_status spec_sync(spec_ctx* c, void* stream) {
+  if (!c) return SPEC_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SPEC_ECUDA;
+  int err = 0;
+  if (cudaMemcpy(&err, c->wk.err, sizeof err, cudaMemcpyDeviceToHost) != cudaSuccess) return SPEC_ECUDA;
+  if (err) {
+    if (cudaMemset(c->wk.err, 0, sizeof(int)) != cudaSuccess) return SPEC_ECUDA;
+    return err == SPEC_ERR_CAPACITY ? SPEC_ECAPACITY : SPEC_EINVAL;
+  }
+  return SPEC_OK;
+}
+
+spec_status spec_set_graphs(spec_ctx* c, int32_t enable) {
+  if (!c) return SPEC_EINVAL;
+  c->graphs = enable != 0;
+  return SPEC_OK;
+}
+
+int64_t spec_kernel_launches(const spec_ctx* c) { return c ? c->launches : 0; }
+
+const char* spec_status_str(spec_status s) {
+  switch (s) {
+    case SPEC_OK: return "ok";
+    case SPEC_EINVAL: return "invalid argument";
+    case SPEC_ECAPACITY: return "capacity exceeded";
+    case SPEC_ESTATE: return "invalid state";
+    case SPEC_ECUDA: return "CUDA error";
+    case SPEC_ETIMEOUT: return "device wait timed out";
+    case SPEC_EUNSUPPORTED: return "unsupported shape";
+  }
+  return "unknown status";
+}
+
+void spec_destroy(spec_ctx* c) {
+  if (!c) return;
+  for (auto& kv : c->cache) cudaGraphExecDestroy(kv.second.exec);
+  delete c;
+}
+
+}  // extern "C"
