@@ -214,10 +214,16 @@ spec_status spec_inject_drafts(spec_ctx *ctx, int32_t B, const int32_t *seq_ids,
  * runs: y[m][n] = sum_k xn[m][k] * W[n][k] for m < M, n < N, where xn = x, or
  * RMSNorm(x) * gain when gain is not NULL. w points to one [N][K] matrix
  * ("device"; for Q4_0 both planes). x ("device" float [M][K]), gain ("device"
- * float [K] or NULL), y ("device" float [M][N]). 1 <= M <= 64. Exposed for
- * kernel-level checks and timing; the passes above call the same kernel. */
+ * float [K] or NULL), y ("device" float [M][N]). 1 <= M <= 64. workspace
+ * ("device", ws_bytes >= spec_linear_workspace_bytes(N, K, M)) holds split-tile
+ * partials and arrival counters; it must be zeroed before its first use and
+ * the kernel leaves it zeroed. Calls sharing a workspace must not overlap.
+ * Exposed for kernel-level checks and timing; the passes above call the same
+ * kernel. */
+size_t spec_linear_workspace_bytes(int32_t N, int32_t K, int32_t M);
 spec_status spec_linear(const spec_matrix *w, int32_t N, int32_t K, const float *x, int32_t M,
-                        const float *gain, float eps, float *y, void *stream);
+                        const float *gain, float eps, float *y, void *workspace, size_t ws_bytes,
+                        void *stream);
 
 /* Copy one slot's counters to the host (synchronises `stream`). */
 spec_status spec_stats(spec_ctx *ctx, int32_t slot, spec_stats_t *out, void *stream);

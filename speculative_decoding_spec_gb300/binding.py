@@ -21,7 +21,8 @@ DTYPES = {F32: 0, BF16: 1, Q4_0: 2}
 
 EXPORTS = ["spec_workspace_bytes", "spec_init", "spec_prefill", "spec_draft", "spec_verify", "spec_step",
            "spec_decode", "spec_inject_drafts", "spec_stats", "spec_sync", "spec_set_graphs",
-           "spec_kernel_launches", "spec_status_str", "spec_destroy", "spec_linear"]
+           "spec_kernel_launches", "spec_status_str", "spec_destroy", "spec_linear",
+           "spec_linear_workspace_bytes"]
 
 
 class spec_matrix(C.Structure):
@@ -107,8 +108,10 @@ def lib():
     L.spec_kernel_launches.argtypes = [p]
     L.spec_status_str.restype = C.c_char_p
     L.spec_status_str.argtypes = [st]
+    L.spec_linear_workspace_bytes.restype = C.c_size_t
+    L.spec_linear_workspace_bytes.argtypes = [i32, i32, i32]
     L.spec_linear.restype = st
-    L.spec_linear.argtypes = [C.POINTER(spec_matrix), i32, i32, p, i32, p, C.c_float, p, p]
+    L.spec_linear.argtypes = [C.POINTER(spec_matrix), i32, i32, p, i32, p, C.c_float, p, p, C.c_size_t, p]
     L.spec_destroy.restype = None
     L.spec_destroy.argtypes = [p]
     _lib = L
@@ -155,9 +158,23 @@ def spec_linear(w, x: torch.Tensor, gain: Optional[torch.Tensor] = None, eps: fl
     if y is None:
         y = torch.empty((M, w.N), dtype=torch.float32, device=x.device)
     s = stream if stream is not None else torch.cuda.current_stream()
+    ws = _linear_ws(x.device, L.spec_linear_workspace_bytes(w.N, w.K, M))
     check("spec_linear", L.spec_linear(C.byref(m), w.N, w.K, _ptr(x), M, _ptr(gain), eps, _ptr(y),
-                                       s.cuda_stream))
+                                       _ptr(ws), ws.numel(), s.cuda_stream))
     return y
+
+
+_LINEAR_WS = {}
+
+
+def _linear_ws(device, nbytes):
+    """A zeroed workspace per device, grown on demand (the kernel leaves it zeroed)."""
+    key = str(device)
+    ws = _LINEAR_WS.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _LINEAR_WS[key] = ws
+    return ws
 
 
 class Engine:

@@ -58,6 +58,15 @@ SPEC_DEV unsigned long long volatile_load(const unsigned long long* p) {
   return *(const volatile unsigned long long*)p;
 }
 
+// Device-scope add with acquire-release ordering: the warp's earlier writes
+// (ordered to lane 0 by a __syncwarp) are visible to whoever observes the new
+// count, and reads after it see every write released before earlier adds.
+SPEC_DEV unsigned int atomic_add_acq_rel(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 SPEC_DEV void set_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }

@@ -479,6 +479,7 @@ int gemv(const GemvArgs& a0, cudaStream_t st) {
     GemvArgs a = a0;
     a.M = std::min(8, a0.M - m0);
     a.X = a0.X + (size_t)m0 * a0.ldx;
+    a.m_base = a0.m_base + m0;
     if (a.Y) a.Y = a0.Y + (size_t)m0 * a0.ldy;
     if (a0.epi == EPI_ARGMAX) {
       a.best = a0.best + m0;
@@ -486,8 +487,8 @@ int gemv(const GemvArgs& a0, cudaStream_t st) {
       if (m0 + 8 < a0.M) a.tail.mode = TAIL_NONE;
     }
     int r = -2;
-    if (a.W.dtype == DT_BF16) r = gemv_tc(a, st);
-    if (r == -1) return -1;
+    if (a.W.dtype == DT_BF16) r = gemv_tc(a, a.tc_fix, a.tc_cnt, st);
+    if (r == -1 || (r == -2 && a.epi == EPI_ROPE)) return -1;
     if (r >= 0) {
       launched += r;
       continue;

@@ -31,7 +31,22 @@ inline Mat mat_layer(Mat m, int l, int N, int K) {
   return m;
 }
 
-enum Epi { EPI_STORE = 0, EPI_ADD = 1, EPI_GEGLU = 2, EPI_ARGMAX = 3 };
+enum Epi { EPI_STORE = 0, EPI_ADD = 1, EPI_GEGLU = 2, EPI_ARGMAX = 3, EPI_ROPE = 4 };
+
+// EPI_ROPE: the QKV projection's epilogue rotates q and k heads (rotate-half
+// RoPE with the pass's cos/sin table), writes rotated q to Y and k, v to the
+// paged cache at each row's position.
+struct RopeEpi {
+  int nq, nkv, hd, R;
+  const float* rope_cs;      // [M][hd/2][2]
+  const int32_t* pos;        // [M]
+  const int32_t* seq_ids;    // [B]
+  void* pool;                // bf16 pool
+  long long layer_off;       // elements to this layer
+  int n_pages, max_pages;
+  const int32_t* block_table;
+  int* err;
+};
 enum Tail { TAIL_NONE = 0, TAIL_VERIFY = 1, TAIL_PREFILL = 2, TAIL_DRAFT = 3 };
 
 // What the last CTA of an argmax launch does once every row's argmax is known.
@@ -66,6 +81,10 @@ struct GemvArgs {
   int geglu_half;           // GEGLU: rows j and j+half pair; Y has `half` columns
   unsigned long long* best; // ARGMAX: [M] packed (score, row) keys, zero before the launch
   TailArgs tail;
+  RopeEpi rope;
+  int m_base;               // absolute index of row 0 of X (row tables of EPI_ROPE)
+  float* tc_fix;            // tensor-core kernel: split-tile partials (gemv_tc_fixup_bytes())
+  unsigned int* tc_cnt;     // tensor-core kernel: per-tile arrival counters, zero between launches
   int pdl;                  // launch with programmatic dependent launch
 };
 int gemv(const GemvArgs& a, cudaStream_t st);
@@ -169,11 +188,17 @@ int inject_drafts(int B, int k, const int32_t* seq_ids, const int32_t* seq_len, 
 // stream capture).
 void setup_gemv_attributes();
 void setup_gemv_tc_attributes();
-int gemv_tc(const GemvArgs& a, cudaStream_t st);
+int gemv_tc(const GemvArgs& a, float* fix, unsigned int* cnt, cudaStream_t st);
+size_t gemv_tc_fixup_bytes();
 void setup_attn_attributes();
 void setup_draft_attributes();
 
 int num_sms();
+// tensor-core attention for bf16 caches (head_dim 64 or 128)
+size_t attention_tc_smem(int hd, int qn);
+void setup_attn_tc_attributes();
+int attention_tc_splits(int B, int nkv, int max_pages, int* pps);
+int attention_tc(const AttnArgs& a, unsigned int* counters, int pps, cudaStream_t st);
 size_t attention_smem(int hd, int qn);
 
 }  // namespace spec

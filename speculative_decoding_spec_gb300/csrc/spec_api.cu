@@ -34,6 +34,9 @@ struct Work {
   int32_t *pos, *sel_row, *n_emit1;
   unsigned long long* best;
   unsigned int* counter;
+  unsigned int* attn_count;
+  float* tc_fix;
+  unsigned int* tc_cnt;
   int* err;
   // drafter
   float *d_cat, *d_u, *d_q, *d_att, *d_act, *d_h, *d_scores, *d_rope, *d_part_o, *d_part_ml;
@@ -44,6 +47,16 @@ struct Work {
 };
 
 constexpr int KMAX = 16;
+
+// Arrival counters of the tensor-core projection: one per 8 output rows of
+// the widest matrix the passes project with.
+size_t tc_counters(const spec_model_desc& m, const spec_drafter_desc* d) {
+  size_t n = std::max<size_t>({(size_t)m.vocab, (size_t)2 * m.d_ff,
+                               (size_t)(m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim, (size_t)m.d_model});
+  if (d) n = std::max<size_t>({n, (size_t)2 * d->d_ff, (size_t)d->n_q_heads * m.head_dim,
+                               (size_t)std::max(d->n_centroids, 1)});
+  return n / 8 + 64;
+}
 
 Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int B_max, int rows_max,
            int max_pages) {
@@ -63,6 +76,9 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
   w.n_emit1 = b.take<int32_t>(base, B_max);
   w.best = b.take<unsigned long long>(base, M);
   w.counter = b.take<unsigned int>(base, 4);
+  w.attn_count = b.take<unsigned int>(base, (size_t)B_max * m.n_kv_heads);
+  w.tc_fix = b.take<float>(base, gemv_tc_fixup_bytes() / sizeof(float));
+  w.tc_cnt = b.take<unsigned int>(base, tc_counters(m, d));
   w.err = b.take<int>(base, 4);
   if (d) {
     const int dq = d->n_q_heads * m.head_dim;
@@ -128,6 +144,7 @@ struct spec_ctx {
   long long layer_elems;
   Work wk;
   bool graphs = true;
+  bool fused_rope = false;
   long long launches = 0;
   struct Entry {
     cudaGraphExec_t exec;
@@ -139,7 +156,21 @@ struct spec_ctx {
 
 namespace {
 
+int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st);
+
 int kv_dt(const spec_ctx* c) { return c->m.kv_dtype == SPEC_F32 ? DT_F32 : DT_BF16; }
+
+// Tensor-core attention for bf16 caches with head_dim 64/128; the CUDA-core
+// kernels otherwise (fp32 caches).
+int run_attention(spec_ctx* c, AttnArgs at, cudaStream_t st) {
+  if (c->m.kv_dtype == SPEC_BF16 && (c->m.head_dim == 64 || c->m.head_dim == 128)) {
+    int pps = 1;
+    at.n_split = attention_tc_splits(at.B, at.nkv, c->kv.max_pages_per_seq, &pps);
+    at.pages_per_split = pps;
+    return attention_tc(at, c->wk.attn_count, pps, st);
+  }
+  return attention(at, st);
+}
 
 // ---- the target pass: rows -> layers -> LM head + argmax + accept -----------
 int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, const int32_t* tokens,
@@ -163,20 +194,30 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
   ra.err = w.err; ra.vocab = m.vocab;
   LAUNCH(embed_rows(ra, st));
 
+  const bool fused_rope = c->fused_rope;
   for (int l = 0; l < m.n_layers; ++l) {
     GemvArgs g = {};
     g.X = w.x; g.ldx = d; g.M = M; g.N = nqkv; g.K = d;
     g.W = mat_layer(M_(c->w.wqkv), l, nqkv, d);
     g.gain = c->w.g_attn + (size_t)l * d; g.eps = m.rms_eps;
     g.epi = EPI_STORE; g.Y = w.qkv; g.ldy = nqkv; g.pdl = 1;
-    LAUNCH(gemv(g, st));
+    if (fused_rope) {
+      g.epi = EPI_ROPE;
+      RopeEpi& e = g.rope;
+      e.nq = nq; e.nkv = nkv; e.hd = hd; e.R = R; e.rope_cs = w.rope_cs; e.pos = w.pos; e.seq_ids = seq_ids;
+      e.pool = c->kv.pool; e.layer_off = (long long)l * c->layer_elems; e.n_pages = c->kv.n_pages;
+      e.max_pages = c->kv.max_pages_per_seq; e.block_table = c->kv.block_table; e.err = w.err;
+    }
+    LAUNCH(run_gemv(c, g, st));
 
+    if (!fused_rope) {
     RopeAppendArgs rp = {};
     rp.qkv = w.qkv; rp.M = M; rp.R = R; rp.nq = nq; rp.nkv = nkv; rp.hd = hd; rp.rope_cs = w.rope_cs;
     rp.pos = w.pos; rp.seq_ids = seq_ids; rp.pool = c->kv.pool; rp.kv_dtype = kv_dt(c);
     rp.layer_elems = c->layer_elems; rp.layer = l; rp.n_pages = c->kv.n_pages;
     rp.max_pages = c->kv.max_pages_per_seq; rp.block_table = c->kv.block_table; rp.err = w.err;
     LAUNCH(rope_append(rp, st));
+    }
 
     AttnArgs at = {};
     at.q = w.qkv; at.ldq = nqkv; at.B = B; at.R = R; at.nq = nq; at.nkv = nkv; at.hd = hd;
@@ -185,26 +226,26 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     at.block_table = c->kv.block_table; at.seq_ids = seq_ids; at.seq_len = c->state.seq_len;
     at.rope_cs = nullptr; at.n_split = c->kv.max_pages_per_seq; at.pages_per_split = 1;
     at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.att; at.err = w.err;
-    LAUNCH(attention(at, st));
+    LAUNCH(run_attention(c, at, st));
 
     g = GemvArgs{};
     g.X = w.att; g.ldx = qd; g.M = M; g.N = d; g.K = qd;
     g.W = mat_layer(M_(c->w.wo), l, d, qd);
     g.epi = EPI_ADD; g.Y = w.x; g.ldy = d; g.pdl = 1;
-    LAUNCH(gemv(g, st));
+    LAUNCH(run_gemv(c, g, st));
 
     g = GemvArgs{};
     g.X = w.x; g.ldx = d; g.M = M; g.N = 2 * ff; g.K = d;
     g.W = mat_layer(M_(c->w.wgu), l, 2 * ff, d);
     g.gain = c->w.g_ffn + (size_t)l * d; g.eps = m.rms_eps;
     g.epi = EPI_GEGLU; g.geglu_half = ff; g.Y = w.act; g.ldy = ff; g.pdl = 1;
-    LAUNCH(gemv(g, st));
+    LAUNCH(run_gemv(c, g, st));
 
     g = GemvArgs{};
     g.X = w.act; g.ldx = ff; g.M = M; g.N = d; g.K = ff;
     g.W = mat_layer(M_(c->w.wdown), l, d, ff);
     g.epi = EPI_ADD; g.Y = w.x; g.ldy = d; g.pdl = 1;
-    LAUNCH(gemv(g, st));
+    LAUNCH(run_gemv(c, g, st));
   }
 
   GemvArgs g = {};
@@ -217,7 +258,7 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
   t.out_tokens = out_tokens; t.n_emitted = n_emitted; t.seq_len = c->state.seq_len;
   t.pending = c->state.pending; t.stats = c->state.stats; t.sel_row = w.sel_row;
   t.best_all = w.best; t.counter = w.counter; t.err = w.err;
-  LAUNCH(gemv(g, st));
+  LAUNCH(run_gemv(c, g, st));
   LAUNCH(commit_hidden(B, seq_ids, w.sel_row, w.x, d, c->w.g_final, m.rms_eps, c->state.hid, st));
   return n;
 }
@@ -242,14 +283,14 @@ int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* dr
     GemvArgs g = {};
     g.X = w.d_cat; g.ldx = 2 * d; g.M = B; g.N = h; g.K = 2 * d; g.W = M_(dw.w_in);
     g.epi = EPI_STORE; g.Y = w.d_u; g.ldy = h; g.pdl = 1;
-    LAUNCH(gemv(g, st));
+    LAUNCH(run_gemv(c, g, st));
 
     for (int l = 0; l < dd.n_layers; ++l) {
       g = GemvArgs{};
       g.X = w.d_u; g.ldx = h; g.M = B; g.N = dq; g.K = h; g.W = mat_layer(M_(dw.wq), l, dq, h);
       g.gain = dw.g_attn + (size_t)l * h; g.eps = m.rms_eps;
       g.epi = EPI_STORE; g.Y = w.d_q; g.ldy = dq; g.pdl = 1;
-      LAUNCH(gemv(g, st));
+      LAUNCH(run_gemv(c, g, st));
 
       AttnArgs at = {};
       at.q = w.d_q; at.ldq = dq; at.B = B; at.R = 1; at.nq = dd.n_q_heads; at.nkv = m.n_kv_heads;
@@ -259,30 +300,30 @@ int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* dr
       at.seq_len = c->state.seq_len; at.rope_cs = w.d_rope; at.n_split = c->kv.max_pages_per_seq;
       at.pages_per_split = 1; at.part_o = w.d_part_o; at.part_ml = w.d_part_ml; at.out = w.d_att;
       at.err = w.err;
-      LAUNCH(attention(at, st));
+      LAUNCH(run_attention(c, at, st));
 
       g = GemvArgs{};
       g.X = w.d_att; g.ldx = dq; g.M = B; g.N = h; g.K = dq; g.W = mat_layer(M_(dw.wo), l, h, dq);
       g.epi = EPI_ADD; g.Y = w.d_u; g.ldy = h; g.pdl = 1;
-      LAUNCH(gemv(g, st));
+      LAUNCH(run_gemv(c, g, st));
 
       g = GemvArgs{};
       g.X = w.d_u; g.ldx = h; g.M = B; g.N = 2 * ff; g.K = h; g.W = mat_layer(M_(dw.wgu), l, 2 * ff, h);
       g.gain = dw.g_ffn + (size_t)l * h; g.eps = m.rms_eps;
       g.epi = EPI_GEGLU; g.geglu_half = ff; g.Y = w.d_act; g.ldy = ff; g.pdl = 1;
-      LAUNCH(gemv(g, st));
+      LAUNCH(run_gemv(c, g, st));
 
       g = GemvArgs{};
       g.X = w.d_act; g.ldx = ff; g.M = B; g.N = h; g.K = ff; g.W = mat_layer(M_(dw.wdown), l, h, ff);
       g.epi = EPI_ADD; g.Y = w.d_u; g.ldy = h; g.pdl = 1;
-      LAUNCH(gemv(g, st));
+      LAUNCH(run_gemv(c, g, st));
     }
 
     // next hidden state h_j = W_out . u
     g = GemvArgs{};
     g.X = w.d_u; g.ldx = h; g.M = B; g.N = d; g.K = h; g.W = M_(dw.w_out);
     g.epi = EPI_STORE; g.Y = w.d_h; g.ldy = d; g.pdl = 1;
-    LAUNCH(gemv(g, st));
+    LAUNCH(run_gemv(c, g, st));
 
     if (!dd.clustered) {
       g = GemvArgs{};
@@ -291,13 +332,13 @@ int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* dr
       TailArgs& t = g.tail;
       t.mode = TAIL_DRAFT; t.B = B; t.R = 1; t.k = k; t.seq_ids = seq_ids; t.draft_out = drafts;
       t.draft_ld = k; t.draft_j = j - 1; t.best_all = w.d_best; t.counter = w.d_counter; t.err = w.err;
-      LAUNCH(gemv(g, st));
+      LAUNCH(run_gemv(c, g, st));
     } else {
       g = GemvArgs{};
       g.X = w.d_u; g.ldx = h; g.M = B; g.N = dd.n_centroids; g.K = h; g.W = M_(dw.centroids);
       g.gain = dw.g_out; g.eps = m.rms_eps; g.epi = EPI_STORE; g.Y = w.d_scores; g.ldy = dd.n_centroids;
       g.pdl = 1;
-      LAUNCH(gemv(g, st));
+      LAUNCH(run_gemv(c, g, st));
       ClusterArgs ca = {};
       ca.B = B; ca.C = dd.n_centroids; ca.top_c = dd.top_c; ca.cs = m.vocab / dd.n_centroids; ca.h = h;
       ca.scores = w.d_scores; ca.chosen = w.d_chosen; ca.u = w.d_u; ca.g_out = dw.g_out; ca.eps = m.rms_eps;
@@ -309,6 +350,12 @@ int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* dr
   }
   return n;
 #undef LAUNCH
+}
+
+int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st) {
+  g.tc_fix = c->wk.tc_fix;
+  g.tc_cnt = c->wk.tc_cnt;
+  return gemv(g, st);
 }
 
 // Run `fn` eagerly, or through a cached CUDA graph keyed by `key`.
@@ -390,7 +437,7 @@ spec_status spec_init(const spec_model_desc* model, const spec_weights* weights,
     if (mm->dtype != m.w_dtype) return SPEC_EINVAL;
   (void)nqkv;
   const int G = m.n_q_heads / m.n_kv_heads;
-  if (attention_smem(m.head_dim, rows_max * G) > 200 * 1024) return SPEC_EUNSUPPORTED;
+  if (attention_smem(m.head_dim, rows_max * G) > 200 * 1024 || rows_max * G > 128) return SPEC_EUNSUPPORTED;
   if (drafter) {
     if (!dweights || !drafter_ok(m, *drafter)) return SPEC_EINVAL;
     const spec_drafter_weights& dw = *dweights;
@@ -421,7 +468,12 @@ spec_status spec_init(const spec_model_desc* model, const spec_weights* weights,
   c->wk = carve((char*)workspace, m, drafter, B_max, rows_max, kv->max_pages_per_seq);
   setup_gemv_attributes();
   setup_attn_attributes();
+  setup_attn_tc_attributes();
   setup_draft_attributes();
+  // RoPE and the KV append run in the QKV projection's epilogue when that
+  // projection is the bf16 tensor-core kernel writing a bf16 cache
+  c->fused_rope = m.w_dtype == SPEC_BF16 && m.kv_dtype == SPEC_BF16 && m.head_dim % 16 == 0 &&
+                  m.d_model % 32 == 0;
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(workspace, 0, need.bytes, st) != cudaSuccess) {
     delete c;
@@ -490,12 +542,20 @@ spec_status spec_inject_drafts(spec_ctx* c, int32_t B, const int32_t* seq_ids, i
   return SPEC_OK;
 }
 
+size_t spec_linear_workspace_bytes(int32_t N, int32_t K, int32_t M) {
+  if (N <= 0 || K <= 0 || M <= 0) return 0;
+  return gemv_tc_fixup_bytes() + (((size_t)N / 8 + 64) * sizeof(unsigned int) + 255) / 256 * 256 + 256;
+}
+
 spec_status spec_linear(const spec_matrix* w, int32_t N, int32_t K, const float* x, int32_t M, const float* gain,
-                        float eps, float* y, void* stream) {
+                        float eps, float* y, void* workspace, size_t ws_bytes, void* stream) {
   if (!w || !x || !y || N <= 0 || K <= 0 || M <= 0 || M > 64 || !mat_ok(*w, K)) return SPEC_EINVAL;
+  if (!workspace || ws_bytes < spec_linear_workspace_bytes(N, K, M)) return SPEC_ECAPACITY;
   GemvArgs g = {};
   g.X = x; g.ldx = K; g.M = M; g.N = N; g.K = K; g.W = M_(*w); g.gain = gain; g.eps = eps;
   g.epi = EPI_STORE; g.Y = y; g.ldy = N; g.pdl = 0;
+  g.tc_fix = (float*)workspace;
+  g.tc_cnt = (unsigned int*)((char*)workspace + gemv_tc_fixup_bytes());
   static std::once_flag once;
   std::call_once(once, setup_gemv_attributes);
   if (gemv(g, (cudaStream_t)stream) < 0) return SPEC_ECUDA;
