@@ -225,6 +225,26 @@ spec_status spec_linear(const spec_matrix *w, int32_t N, int32_t K, const float 
                         const float *gain, float eps, float *y, void *workspace, size_t ws_bytes,
                         void *stream);
 
+/* spec_linear without a caller workspace, for callers that cannot allocate
+ * device memory (a host application that owns the whole device-memory budget,
+ * a plugin whose framework allocator must see every allocation, code that must
+ * not reach cudaMalloc because it can synchronise the device). The pages have
+ * no counterpart of this call: it only moves spec_linear's scratch (split-tile
+ * partials and arrival counters) into a fixed 512 KiB array in the library's
+ * device image, held by every GPU that loads the library until the process
+ * exits. Same arguments and results as spec_linear otherwise.
+ *  - N may be at most SPEC_LINEAR_NOALLOC_MAX_ROWS; larger N returns
+ *    SPEC_ECAPACITY without launching anything.
+ *  - The first call on a device looks up the array's address with that device
+ *    current; make it before any stream capture.
+ *  - All calls share the array: calls that overlap on the GPU (other streams,
+ *    other host threads) race on it and must be serialised by the caller.
+ *  - The counters are cleared on `stream` at the start of every call.
+ * Allocates nothing (no cudaMalloc / cudaFree, no allocating library call). */
+#define SPEC_LINEAR_NOALLOC_MAX_ROWS 523776
+spec_status spec_linear_noalloc(const spec_matrix *w, int32_t N, int32_t K, const float *x, int32_t M,
+                                const float *gain, float eps, float *y, void *stream);
+
 /* Copy one slot's counters to the host (synchronises `stream`). */
 spec_status spec_stats(spec_ctx *ctx, int32_t slot, spec_stats_t *out, void *stream);
 

@@ -22,7 +22,8 @@ DTYPES = {F32: 0, BF16: 1, Q4_0: 2}
 EXPORTS = ["spec_workspace_bytes", "spec_init", "spec_prefill", "spec_draft", "spec_verify", "spec_step",
            "spec_decode", "spec_inject_drafts", "spec_stats", "spec_sync", "spec_set_graphs",
            "spec_kernel_launches", "spec_status_str", "spec_destroy", "spec_linear",
-           "spec_linear_workspace_bytes"]
+           "spec_linear_workspace_bytes", "spec_linear_noalloc"]
+SPEC_LINEAR_NOALLOC_MAX_ROWS = 523776
 
 
 class spec_matrix(C.Structure):
@@ -112,6 +113,8 @@ def lib():
     L.spec_linear_workspace_bytes.argtypes = [i32, i32, i32]
     L.spec_linear.restype = st
     L.spec_linear.argtypes = [C.POINTER(spec_matrix), i32, i32, p, i32, p, C.c_float, p, p, C.c_size_t, p]
+    L.spec_linear_noalloc.restype = st
+    L.spec_linear_noalloc.argtypes = [C.POINTER(spec_matrix), i32, i32, p, i32, p, C.c_float, p, p]
     L.spec_destroy.restype = None
     L.spec_destroy.argtypes = [p]
     _lib = L
@@ -161,6 +164,22 @@ def spec_linear(w, x: torch.Tensor, gain: Optional[torch.Tensor] = None, eps: fl
     ws = _linear_ws(x.device, L.spec_linear_workspace_bytes(w.N, w.K, M))
     check("spec_linear", L.spec_linear(C.byref(m), w.N, w.K, _ptr(x), M, _ptr(gain), eps, _ptr(y),
                                        _ptr(ws), ws.numel(), s.cuda_stream))
+    return y
+
+
+def spec_linear_noalloc(w, x: torch.Tensor, gain: Optional[torch.Tensor] = None, eps: float = 1e-6,
+                        layer: int = 0, y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """spec_linear through the entry point that allocates nothing (its scratch
+    is a fixed array inside the library; see include/spec.h)."""
+    L = lib()
+    sub = synth.WTensor(w.dtype, 1, w.N, w.K, w.data[layer], w.scales[layer] if w.scales is not None else None)
+    m = _mat(sub)
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, w.N), dtype=torch.float32, device=x.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    check("spec_linear_noalloc", L.spec_linear_noalloc(C.byref(m), w.N, w.K, _ptr(x), M, _ptr(gain), eps,
+                                                       _ptr(y), s.cuda_stream))
     return y
 
 
