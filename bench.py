@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 
 from speculative_decoding_spec_gb300 import configs, synth  # noqa: E402
 
+PERSISTENT = 0
 METRIC = "verify tok/s and HBM GB/s (% of roofline); effective tok/s at set acceptance"
 UNIT = "tok/s"
 
@@ -108,7 +109,7 @@ def setup_workload(w: configs.Workload, steps_total: int, device):
     ctx = synth.make_context_lengths(w.B, *w.ctx)
     grow = steps_total * (w.k + 1) + w.k + 2
     eng = binding.Engine(tw, dw, n_slots=w.B, B_max=w.B, rows_max=w.k + 1, max_ctx=max(ctx) + grow + 64,
-                         shuffle_pages=w.ctx[0] != w.ctx[1])
+                         shuffle_pages=w.ctx[0] != w.ctx[1], persistent=bool(PERSISTENT))
     for b in range(w.B):
         eng.load_prefilled(b, synth.make_prefilled_kv(t, ctx[b] - 1, device=device, seed=synth.SEED_KV + b))
     first = synth.make_tokens(w.B, t.V, device=device).view(w.B, 1)
@@ -302,6 +303,7 @@ def run_gpu(args, w, rank, world):
                      "frac": gb_avg / (gms / 1e3) / 1e9 / hbm_peak, "peak_kind": peak_kind,
                      "bytes_per_launch": gb_avg, "ms_per_launch": gms, "traffic": None},
         "gpu_launches": launches,
+        "persistent_pass": bool(PERSISTENT),
         "clocks": ck,
     }
     return res, tw, eng, ctx
@@ -360,7 +362,11 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=20.0)
+    ap.add_argument("--persistent", type=int, default=0,
+                    help="1: one persistent kernel per target pass; 0: one kernel per step")
     args = ap.parse_args()
+    global PERSISTENT
+    PERSISTENT = args.persistent
     args.warmup = max(args.warmup, 3)
     w = configs.WORKLOADS[args.workload]
 

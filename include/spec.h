@@ -255,6 +255,29 @@ spec_status spec_sync(spec_ctx *ctx, void *stream);
  * for non-NULL streams). */
 spec_status spec_set_graphs(spec_ctx *ctx, int32_t enable);
 
+/* Execution options (for comparisons; both default to 1):
+ *  SPEC_OPT_GRAPHS      capture each call shape in a CUDA graph and replay it;
+ *  SPEC_OPT_PERSISTENT  run a bf16 target pass of at most 8 rows as one
+ *                       persistent kernel (all SMs walk the pass's steps with a
+ *                       bounded grid barrier between them) instead of one
+ *                       kernel per step;
+ *  SPEC_OPT_TRACE       value = a device pointer to a uint64 buffer of at least
+ *                       (3 + 5*n_layers) * n_SMs * 6 entries, or 0: the
+ *                       persistent pass records, per step and CTA, the step's
+ *                       start, two marks inside a projection step (activations
+ *                       staged, main loop done), the end of the step's work
+ *                       and the arrival at the barrier after it (globaltimer,
+ *                       ns; slot 5 unused).
+ * Changing an option drops the captured graphs. */
+#define SPEC_OPT_GRAPHS 1
+#define SPEC_OPT_PERSISTENT 2
+#define SPEC_OPT_TRACE 3
+/*  SPEC_OPT_PREFETCH    (default 1) in the persistent pass, each CTA pulls its
+ *                       share of the next step's weights or KV pages towards
+ *                       L2 before the grid barrier. */
+#define SPEC_OPT_PREFETCH 4
+spec_status spec_set_option(spec_ctx *ctx, int32_t option, int64_t value);
+
 /* Number of kernels the library launched (or replayed inside graphs) since the
  * context was created. */
 int64_t spec_kernel_launches(const spec_ctx *ctx);

@@ -22,7 +22,8 @@ DTYPES = {F32: 0, BF16: 1, Q4_0: 2}
 EXPORTS = ["spec_workspace_bytes", "spec_init", "spec_prefill", "spec_draft", "spec_verify", "spec_step",
            "spec_decode", "spec_inject_drafts", "spec_stats", "spec_sync", "spec_set_graphs",
            "spec_kernel_launches", "spec_status_str", "spec_destroy", "spec_linear",
-           "spec_linear_workspace_bytes", "spec_linear_noalloc"]
+           "spec_linear_workspace_bytes", "spec_linear_noalloc", "spec_set_option"]
+SPEC_OPT_GRAPHS, SPEC_OPT_PERSISTENT, SPEC_OPT_TRACE, SPEC_OPT_PREFETCH = 1, 2, 3, 4
 SPEC_LINEAR_NOALLOC_MAX_ROWS = 523776
 
 
@@ -113,6 +114,8 @@ def lib():
     L.spec_linear_workspace_bytes.argtypes = [i32, i32, i32]
     L.spec_linear.restype = st
     L.spec_linear.argtypes = [C.POINTER(spec_matrix), i32, i32, p, i32, p, C.c_float, p, p, C.c_size_t, p]
+    L.spec_set_option.restype = st
+    L.spec_set_option.argtypes = [p, i32, C.c_int64]
     L.spec_linear_noalloc.restype = st
     L.spec_linear_noalloc.argtypes = [C.POINTER(spec_matrix), i32, i32, p, i32, p, C.c_float, p, p]
     L.spec_destroy.restype = None
@@ -201,7 +204,7 @@ class Engine:
     around one spec_ctx and forwards calls to the C ABI on its own stream."""
 
     def __init__(self, tw, dw=None, n_slots=1, B_max=1, rows_max=4, max_ctx=256, shuffle_pages=False,
-                 device="cuda", graphs=True):
+                 device="cuda", graphs=True, persistent=False):
         L = lib()
         t = tw.shape
         self.tw, self.dw, self.shape = tw, dw, t
@@ -247,6 +250,7 @@ class Engine:
         self.ctx = ctx
         if not graphs:
             check("spec_set_graphs", L.spec_set_graphs(ctx, 0))
+        check("spec_set_option", L.spec_set_option(ctx, SPEC_OPT_PERSISTENT, int(bool(persistent))))
         self._bufs = {}
 
     # -- helpers ------------------------------------------------------------
@@ -332,6 +336,9 @@ class Engine:
         s = spec_stats_t()
         check("spec_stats", lib().spec_stats(self.ctx, slot, C.byref(s), self.stream.cuda_stream))
         return s
+
+    def set_option(self, option: int, value: int):
+        check("spec_set_option", lib().spec_set_option(self.ctx, option, int(value)))
 
     def kernel_launches(self) -> int:
         return lib().spec_kernel_launches(self.ctx)

@@ -67,6 +67,15 @@ SPEC_DEV unsigned int atomic_add_acq_rel(unsigned int* p, unsigned int v) {
   return old;
 }
 
+SPEC_DEV unsigned int ld_acquire(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+SPEC_DEV void st_release(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 SPEC_DEV void set_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }

@@ -1,0 +1,505 @@
+// gemv_tc.cuh -- weight-streaming projection for bf16 weights on the tensor
+// cores (mma.sync m16n8k16, fp32 accumulate), for M <= 8 rows per pass.
+//
+// The verify pass reads every weight once for the k+1 rows of each sequence
+// ("Gemma 4's MTP drafter explained" (molayo1419.me), section "Why is
+// generating one token at a time slow?"), so this kernel is bound by HBM: the
+// tensor cores only remove the per-element ALU cost of the CUDA-core version.
+//
+// Fragments. A warp owns a 16-row weight tile. Lane (g = lane/4, c = lane%4)
+// loads 16 bytes (8 consecutive bf16) of tile rows g and g+8 per 32-column
+// step; those 8 columns feed two k16 MMAs through a fixed permutation of the
+// reduction index (k-slot 2c+j <-> column 8c+j, 2c+8+j <-> 8c+2+j, then the
+// next 4 columns), and the activation fragment of row n = g is the same 16
+// bytes of X[g] in shared memory. The output fragment holds rows g and g+8 of
+// the tile for m = 2c, 2c+1, so a pair of weight rows that must meet in the
+// epilogue (gate/up of a GELU-gated FFN) is mapped to g and g+8.
+//
+// Precision. X is held as bf16 hi + lo (x = hi + lo to 2^-17 relative) and
+// each step runs two MMAs, so the result matches an fp32-activation dot
+// product of the exact bf16 weights. Each row's result depends only on that
+// row and X, never on M.
+//
+// Work split. Persistent CTAs of 16 warps; CTA c owns a balanced range of row
+// tiles. When a CTA has fewer tiles than warps, K is cut into slices and the
+// slice partials are added in a fixed order; when X does not fit in shared
+// memory, K is staged in chunks (each chunk a further set of slices).
+#pragma once
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "tail.cuh"
+
+#define HOSTDEV_INLINE __host__ __forceinline__
+
+namespace spec {
+namespace tc {
+
+constexpr int TW_DEFAULT = 16;          // warps per CTA of the stand-alone kernel
+constexpr int XPAD = 32;                // bf16 pad per staged row (64 B): conflict-free 16-byte reads
+constexpr int SMEM_MAX = 227 * 1024;
+
+enum { MAP_PLAIN = 0, MAP_PAIR = 1, MAP_ROPE = 2 };
+
+struct SkPlan {
+  int T;         // 16-row output tiles
+  int C;         // 128-column K chunks
+  int U;         // units = T * C, tile-major
+  int grid;
+  int Ms;        // staged activation rows (= M)
+  int xs;        // staged row stride (bf16 elements)
+  size_t smem;
+};
+
+constexpr int KCH = 128;   // columns per unit (4 k-steps of 32)
+
+static SPEC_DEV void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                       uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+static SPEC_DEV uint32_t bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// first unit of CTA b
+__device__ HOSTDEV_INLINE int unit_begin(int b, const SkPlan& p) { return (int)(((long long)b * p.U) / p.grid); }
+
+template <int TW>
+struct Sk {
+  const GemvArgs& a;
+  const SkPlan& p;
+  int map;
+  uint16_t *xhi, *xlo;
+  float* seg;               // [TW][2][32][4] flushed partial segments
+  int* seg_tag;             // [TW][2]: tile, or -1
+  int* seg_c0;              // [TW][2]: first chunk of the segment
+  int* seg_c1;              // [TW][2]: one past the last chunk
+  float* inv_rms;           // [8]
+  float* red;               // [TW][8] norm partials
+  unsigned long long* best; // [TW][8]
+  int* flag;
+  float* fix;               // global [grid][2][32][4]
+  unsigned int* cnt;        // global [T]
+  int bid;                  // this CTA's index in the launch (or phase)
+  bool standalone;          // own launch (PDL waits) or a phase of the persistent pass kernel
+  unsigned long long* trace;  // optional: [0] after staging, [1] after the main loop
+
+  // MAP_ROPE: tile t covers elements 8u..8u+7 of head h (row g) and the
+  // elements hd/2 further on (row g+8), the pairs RoPE rotates together
+  SPEC_DEV int row_g(int t, int g) const {
+    if (map == MAP_ROPE) {
+      const int hpt = a.rope.hd / 16;
+      return (t / hpt) * a.rope.hd + 8 * (t % hpt) + g;
+    }
+    return map == MAP_PAIR ? 8 * t + g : 16 * t + g;
+  }
+  SPEC_DEV int row_g8(int t, int g) const {
+    if (map == MAP_ROPE) return row_g(t, g) + a.rope.hd / 2;
+    return map == MAP_PAIR ? a.geglu_half + 8 * t + g : 16 * t + 8 + g;
+  }
+  SPEC_DEV bool ok_g(int t, int g) const { return map == MAP_PAIR ? 8 * t + g < a.geglu_half : 16 * t + g < a.N; }
+  SPEC_DEV bool ok_g8(int t, int g) const {
+    return map == MAP_PAIR ? 8 * t + g < a.geglu_half : 16 * t + 8 + g < a.N;
+  }
+
+  // Issue the 8 weight loads of unit u (rows g and g+8 of its tile, 4 k-steps).
+  SPEC_DEV void load_unit(int u, uint4 (&wa)[4], uint4 (&wb)[4]) const {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int t = u / p.C, ch = u - t * p.C;
+    const int k0 = ch * KCH, steps = min(4, (a.K - k0) / 32);
+    const bool vg = ok_g(t, g), vg8 = ok_g8(t, g);
+    const __nv_bfloat16* W = (const __nv_bfloat16*)a.W.data;
+    const __nv_bfloat16* rg = W + (size_t)(vg ? row_g(t, g) : 0) * a.K + k0 + 8 * q;
+    const __nv_bfloat16* rg8 = W + (size_t)(vg8 ? row_g8(t, g) : 0) * a.K + k0 + 8 * q;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      wa[s] = (vg && s < steps) ? ldg_stream(rg + s * 32) : make_uint4(0, 0, 0, 0);
+      wb[s] = (vg8 && s < steps) ? ldg_stream(rg8 + s * 32) : make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  // prefetch.global.L2 of the weight lines of units [u0, u1), at most 256 KB
+  SPEC_DEV void prefetch_slice(int u0, int u1) const {
+    const int per_unit = 32;  // 16 rows x 2 lines of 128 B (a unit is 128 columns)
+    const int n = min((u1 - u0) * per_unit, 2048);
+    const __nv_bfloat16* W = (const __nv_bfloat16*)a.W.data;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int u = u0 + i / per_unit, r = (i % per_unit) >> 1, half = i & 1;
+      const int t = u / p.C, ch = u - t * p.C;
+      const int g = r & 7;
+      const bool hi_row = r >= 8;
+      if (!(hi_row ? ok_g8(t, g) : ok_g(t, g))) continue;
+      const int row = hi_row ? row_g8(t, g) : row_g(t, g);
+      const int col = ch * KCH + half * 64;
+      if (col < a.K) prefetch_l2(W + (size_t)row * a.K + col);
+    }
+  }
+
+  SPEC_DEV void mma_unit(int u, const uint4 (&wa)[4], const uint4 (&wb)[4], float (&c)[4]) const {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int ch = u % p.C, k0 = ch * KCH, steps = min(4, (a.K - k0) / 32);
+    const bool xrow = g < p.Ms;
+    const uint16_t* bh = xhi + g * p.xs + k0 + 8 * q;
+    const uint16_t* bl = xlo + g * p.xs + k0 + 8 * q;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      if (s >= steps) break;
+      uint4 xh = make_uint4(0, 0, 0, 0), xl = make_uint4(0, 0, 0, 0);
+      if (xrow) {
+        xh = *reinterpret_cast<const uint4*>(bh + s * 32);
+        xl = *reinterpret_cast<const uint4*>(bl + s * 32);
+      }
+      mma16816(c, wa[s].x, wb[s].x, wa[s].y, wb[s].y, xh.x, xh.y);
+      mma16816(c, wa[s].x, wb[s].x, wa[s].y, wb[s].y, xl.x, xl.y);
+      mma16816(c, wa[s].z, wb[s].z, wa[s].w, wb[s].w, xh.z, xh.w);
+      mma16816(c, wa[s].z, wb[s].z, wa[s].w, wb[s].w, xl.z, xl.w);
+    }
+  }
+
+  // Stage X*gain as bf16 hi/lo planes (all of K, M rows) and the row norms:
+  // RMSNorm's 1/rms is a per-row factor, applied in the epilogue.
+  SPEC_DEV void stage() {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per_row = a.K / 8;
+    const int items = p.Ms * per_row;
+    constexpr int BATCH = TW >= 16 ? 4 : 8;  // items per thread whose loads are all in flight together
+    float ss[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) ss[m] = 0.f;
+    for (int base = 0; base < items; base += BATCH * blockDim.x) {
+      float4 u0[BATCH], u1[BATCH];
+#pragma unroll
+      for (int j = 0; j < BATCH; ++j) {
+        const int idx = base + j * blockDim.x + threadIdx.x;
+        if (idx < items) {
+          const int m = idx / per_row, c8 = (idx - m * per_row) * 8;
+          // activations come from other CTAs of the same persistent launch: L2 only
+          u0[j] = __ldcg(reinterpret_cast<const float4*>(a.X + (size_t)m * a.ldx + c8));
+          u1[j] = __ldcg(reinterpret_cast<const float4*>(a.X + (size_t)m * a.ldx + c8 + 4));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < BATCH; ++j) {
+        const int idx = base + j * blockDim.x + threadIdx.x;
+        if (idx >= items) continue;
+        const int m = idx / per_row, c8 = (idx - m * per_row) * 8;
+        float v[8] = {u0[j].x, u0[j].y, u0[j].z, u0[j].w, u1[j].x, u1[j].y, u1[j].z, u1[j].w};
+        if (a.gain) {
+          float sq = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) sq = fmaf(v[i], v[i], sq);
+#pragma unroll
+          for (int mm = 0; mm < 8; ++mm)
+            if (mm == m) ss[mm] += sq;
+          const float4 g0 = *reinterpret_cast<const float4*>(a.gain + c8);
+          const float4 g1 = *reinterpret_cast<const float4*>(a.gain + c8 + 4);
+          v[0] *= g0.x; v[1] *= g0.y; v[2] *= g0.z; v[3] *= g0.w;
+          v[4] *= g1.x; v[5] *= g1.y; v[6] *= g1.z; v[7] *= g1.w;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
+          hi[i] = bf16x2(v[2 * i], v[2 * i + 1]);
+          lo[i] = bf16x2(v[2 * i] - __bfloat162float(h0), v[2 * i + 1] - __bfloat162float(h1));
+        }
+        *reinterpret_cast<uint4*>(xhi + m * p.xs + c8) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(xlo + m * p.xs + c8) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+    if (a.gain) {
+      // fixed-order reduction: lanes, then warps
+      for (int m = 0; m < p.Ms; ++m) {
+        const float v = warp_sum(ss[m]);
+        if (lane == 0) red[warp * 8 + m] = v;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < 8) {
+      float inv = 1.f;
+      if (a.gain && (int)threadIdx.x < p.Ms) {
+        float t = 0.f;
+        for (int w = 0; w < TW; ++w) t += red[w * 8 + threadIdx.x];
+        inv = rsqrtf(t / (float)a.K + a.eps);
+      }
+      inv_rms[threadIdx.x] = inv;
+    }
+    __syncthreads();
+  }
+
+  SPEC_DEV void finish(int t, float (&c)[4], unsigned long long (&mybest)[2]) {
+    const int q = (threadIdx.x & 31) & 3;
+    const float s0 = inv_rms[2 * q], s1 = inv_rms[2 * q + 1];
+    c[0] *= s0; c[1] *= s1; c[2] *= s0; c[3] *= s1;
+    epilogue(t, c, mybest);
+  }
+
+  SPEC_DEV void epilogue(int t, const float (&c)[4], unsigned long long (&mybest)[2]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int m0 = 2 * q, m1 = 2 * q + 1;
+    if (map == MAP_ROPE) {
+      const RopeEpi& e = a.rope;
+      const int hpt = e.hd / 16, h = t / hpt, j = 8 * (t % hpt) + g, half = e.hd / 2;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int m = 2 * q + i;
+        if (m >= a.M) continue;
+        const int am = a.m_base + m;
+        float y0 = c[i], y1 = c[2 + i];
+        if (h < e.nq + e.nkv) {
+          const float co = __ldcg(e.rope_cs + (size_t)am * e.hd + 2 * j);
+          const float si = __ldcg(e.rope_cs + (size_t)am * e.hd + 2 * j + 1);
+          const float x0 = y0, x1 = y1;
+          y0 = x0 * co - x1 * si;
+          y1 = x1 * co + x0 * si;
+        }
+        if (h < e.nq) {
+          a.Y[(size_t)m * a.ldy + h * e.hd + j] = y0;
+          a.Y[(size_t)m * a.ldy + h * e.hd + j + half] = y1;
+        } else {
+          const int pos = __ldcg(e.pos + am), slot = e.seq_ids[am / e.R], pidx = pos / 64;
+          const int page = pidx < e.max_pages ? e.block_table[(size_t)slot * e.max_pages + pidx] : -1;
+          if (page < 0 || page >= e.n_pages) {
+            set_error(e.err, SPEC_ERR_CAPACITY);
+            continue;
+          }
+          const int plane = h < e.nq + e.nkv ? 0 : 1;
+          const int kh = h - e.nq - plane * e.nkv;
+          __nv_bfloat16* dst = (__nv_bfloat16*)e.pool + e.layer_off +
+                               ((((size_t)page * 2 + plane) * e.nkv + kh) * 64 + pos % 64) * e.hd;
+          dst[j] = __float2bfloat16_rn(y0);
+          dst[j + half] = __float2bfloat16_rn(y1);
+        }
+      }
+      return;
+    }
+    if (map == MAP_PAIR) {
+      if (!ok_g(t, g)) return;
+      const int j = 8 * t + g;
+      auto gl = [](float x) { return 0.5f * x * (1.f + erff(x * 0.70710678118654752f)); };
+      if (m0 < a.M) a.Y[(size_t)m0 * a.ldy + j] = gl(c[0]) * c[2];
+      if (m1 < a.M) a.Y[(size_t)m1 * a.ldy + j] = gl(c[1]) * c[3];
+      return;
+    }
+    const int rows[2] = {row_g(t, g), row_g8(t, g)};
+    const bool oks[2] = {ok_g(t, g), ok_g8(t, g)};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (!oks[h]) continue;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int m = 2 * q + i;
+        if (m >= a.M) continue;
+        const float v = c[2 * h + i];
+        float* y = a.Y ? a.Y + (size_t)m * a.ldy + rows[h] : nullptr;
+        if (a.epi == EPI_STORE) *y = v;
+        else if (a.epi == EPI_ADD) *y = __ldcg(y) + v;
+        else {
+          if (y) *y = v;
+          const unsigned long long key = pack_best(v, (uint32_t)rows[h]);
+          mybest[i] = key > mybest[i] ? key : mybest[i];
+        }
+      }
+    }
+  }
+
+  SPEC_DEV void run() {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int b = bid;
+    const int u0 = unit_begin(b, p), u1 = unit_begin(b + 1, p);
+    const int nu = u1 - u0;
+    const int wa_ = u0 + (int)(((long long)warp * nu) / TW), wb_ = u0 + (int)(((long long)(warp + 1) * nu) / TW);
+
+    // weights do not depend on the previous kernel: pull this CTA's slice
+    // towards L2 (capped) and put the first unit in flight before the wait
+    uint4 wa[4], wb[4];
+    if (standalone) {
+      prefetch_slice(u0, u1);
+      if (wa_ < wb_) load_unit(wa_, wa, wb);
+      grid_dep_wait();
+      grid_dep_launch();
+    }
+    if (threadIdx.x < TW * 2) seg_tag[threadIdx.x] = -1;
+    stage();
+    // in the persistent pass the slice was pulled to L2 before the barrier;
+    // first weight loads only now, so they do not queue ahead of the staging
+    if (!standalone && wa_ < wb_) load_unit(wa_, wa, wb);
+    if (trace && threadIdx.x == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(trace[0]));
+
+    unsigned long long mybest[2] = {0ull, 0ull};
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    int nseg = 0;
+    int seg_start = wa_;
+    for (int u = wa_; u < wb_; ++u) {
+      uint4 ca[4], cb[4];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        ca[s] = wa[s];
+        cb[s] = wb[s];
+      }
+      if (u + 1 < wb_) load_unit(u + 1, wa, wb);  // next unit in flight
+      mma_unit(u, ca, cb, c);
+      const int t = u / p.C;
+      const bool tile_end = u + 1 == wb_ || (u + 1) / p.C != t;
+      if (tile_end) {
+        const int c0 = seg_start - t * p.C, c1 = u + 1 - t * p.C;
+        if (c0 == 0 && c1 == p.C) {
+          finish(t, c, mybest);
+        } else {
+          // a warp range holds at most two partial tiles: its first and its last
+          const int slot = warp * 2 + (nseg > 0 ? 1 : 0);
+          reinterpret_cast<float4*>(seg)[slot * 32 + lane] = make_float4(c[0], c[1], c[2], c[3]);
+          if (lane == 0) {
+            seg_tag[slot] = t;
+            seg_c0[slot] = c0;
+            seg_c1[slot] = c1;
+          }
+        }
+        ++nseg;
+        c[0] = c[1] = c[2] = c[3] = 0.f;
+        seg_start = u + 1;
+      }
+    }
+    __syncthreads();
+    if (trace && threadIdx.x == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(trace[1]));
+
+    // partial tiles of this CTA: add segments in chunk order; a tile whole in
+    // this CTA is finished here, one shared with neighbours goes to the fixup.
+    // Slots are in (warp, first/last) order, i.e. in tile and chunk order, so a
+    // tile's segments are consecutive valid slots; each group starts at a slot
+    // whose previous valid slot holds another tile.
+    const int t_first = u0 / p.C;
+    if (nu > 0) {
+      for (int sl0 = warp; sl0 < TW * 2; sl0 += TW) {
+        const int tt = seg_tag[sl0];
+        if (tt < 0) continue;
+        int prev = sl0 - 1;
+        while (prev >= 0 && seg_tag[prev] < 0) --prev;
+        if (prev >= 0 && seg_tag[prev] == tt) continue;  // not the first segment of its tile
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int sl = sl0; sl < TW * 2; ++sl) {
+          const int tg = seg_tag[sl];
+          if (tg < 0) continue;
+          if (tg != tt) break;
+          const float4 v = reinterpret_cast<const float4*>(seg)[sl * 32 + lane];
+          acc[0] += v.x; acc[1] += v.y; acc[2] += v.z; acc[3] += v.w;
+        }
+        const int tb = tt * p.C, te = tb + p.C;
+        if (tb >= u0 && te <= u1) {
+          finish(tt, acc, mybest);
+          continue;
+        }
+        // shared with other CTAs: publish, and the last contributor finishes
+        const int slot = tt == t_first ? 0 : 1;
+        reinterpret_cast<float4*>(fix)[((size_t)b * 2 + slot) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncwarp();
+        unsigned int done = 0;
+        const int b_first = cta_of(tb), b_lastc = cta_of(te - 1);
+        if (lane == 0) done = atomic_add_acq_rel(cnt + tt, 1u);
+        done = __shfl_sync(FULL, done, 0);
+        if ((int)done != b_lastc - b_first) continue;
+        float tot[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int bb = b_first; bb <= b_lastc; ++bb) {
+          const int s2 = tt == unit_begin(bb, p) / p.C ? 0 : 1;
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(fix) + ((size_t)bb * 2 + s2) * 32 + lane);
+          tot[0] += v.x; tot[1] += v.y; tot[2] += v.z; tot[3] += v.w;
+        }
+        if (lane == 0) cnt[tt] = 0u;
+        finish(tt, tot, mybest);
+      }
+    }
+    if (a.epi == EPI_ARGMAX) argmax_tail(mybest);
+  }
+
+  // CTA whose unit range holds unit u
+  SPEC_DEV int cta_of(int u) const {
+    int bb = (int)((((long long)u + 1) * p.grid - 1) / p.U);
+    while (bb > 0 && unit_begin(bb, p) > u) --bb;
+    while (bb + 1 < p.grid && unit_begin(bb + 1, p) <= u) ++bb;
+    return bb;
+  }
+
+  SPEC_DEV void argmax_tail(unsigned long long (&mybest)[2]) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const unsigned long long other = __shfl_xor_sync(FULL, mybest[i], o);
+        mybest[i] = other > mybest[i] ? other : mybest[i];
+      }
+    if (lane < 4) {
+      best[warp * 8 + 2 * lane] = mybest[0];
+      best[warp * 8 + 2 * lane + 1] = mybest[1];
+    }
+    __syncthreads();
+    if (threadIdx.x < a.M) {
+      unsigned long long bst = 0ull;
+      for (int w = 0; w < TW; ++w) bst = best[w * 8 + threadIdx.x] > bst ? best[w * 8 + threadIdx.x] : bst;
+      if (bst) atomicMax(&a.best[threadIdx.x], bst);
+    }
+    if (a.tail.mode == TAIL_NONE) return;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned int done = atomicAdd(a.tail.counter, 1u);
+      *flag = done == (unsigned int)p.grid - 1;
+    }
+    __syncthreads();
+    if (!*flag) return;
+    __threadfence();
+    run_tail(a.tail);
+  }
+};
+
+__host__ __device__ inline int map_of(int epi) {
+  return epi == EPI_GEGLU ? MAP_PAIR : epi == EPI_ROPE ? MAP_ROPE : MAP_PLAIN;
+}
+
+// Stream-K plan: T tiles x C chunks spread over min(U, nsm) CTAs of TW warps.
+template <int TW = 16>
+__host__ __device__ inline SkPlan plan(const GemvArgs& a, int map, int nsm) {
+  SkPlan p;
+  p.T = map == MAP_PAIR ? (a.geglu_half + 7) / 8 : map == MAP_ROPE ? a.N / 16 : (a.N + 15) / 16;
+  p.C = (a.K + KCH - 1) / KCH;
+  p.U = p.T * p.C;
+  p.grid = p.U < nsm ? p.U : nsm;
+  p.Ms = a.M;
+  p.xs = a.K + XPAD;
+  const size_t xb = (size_t)(p.Ms > 1 ? p.Ms : 1) * p.xs * 2 * 2;
+  p.smem = xb + (size_t)TW * 2 * 32 * 16 + TW * 2 * 3 * 4 + 8 * 4 + TW * 8 * 4 + TW * 8 * 8 + 16;
+  return p;
+}
+
+// Carve the dynamic shared memory for a projection CTA.
+template <int TW>
+__device__ inline void sk_bind(Sk<TW>& k, unsigned char* smem_raw, float* fix, unsigned int* cnt, int bid,
+                               bool standalone) {
+  const SkPlan& p = k.p;
+  k.xhi = reinterpret_cast<uint16_t*>(smem_raw);
+  k.xlo = k.xhi + (size_t)(p.Ms > 1 ? p.Ms : 1) * p.xs;
+  k.seg = reinterpret_cast<float*>(k.xlo + (size_t)(p.Ms > 1 ? p.Ms : 1) * p.xs);
+  k.seg_tag = reinterpret_cast<int*>(k.seg + TW * 2 * 32 * 4);
+  k.seg_c0 = k.seg_tag + TW * 2;
+  k.seg_c1 = k.seg_c0 + TW * 2;
+  k.inv_rms = reinterpret_cast<float*>(k.seg_c1 + TW * 2);
+  k.red = k.inv_rms + 8;
+  k.best = reinterpret_cast<unsigned long long*>(k.red + TW * 8);
+  k.flag = reinterpret_cast<int*>(k.best + TW * 8);
+  k.fix = fix;
+  k.cnt = cnt;
+  k.bid = bid;
+  k.standalone = standalone;
+  k.trace = nullptr;
+}
+
+}  // namespace tc
+}  // namespace spec

@@ -10,7 +10,7 @@ namespace spec {
 enum { DT_F32 = 0, DT_BF16 = 1, DT_Q4_0 = 2 };
 
 // Device error word values (first error wins).
-enum { SPEC_ERR_NONE = 0, SPEC_ERR_TOKEN = 1, SPEC_ERR_CAPACITY = 2, SPEC_ERR_REF = 3 };
+enum { SPEC_ERR_NONE = 0, SPEC_ERR_TOKEN = 1, SPEC_ERR_CAPACITY = 2, SPEC_ERR_REF = 3, SPEC_ERR_TIMEOUT = 4 };
 
 // One row-major matrix [N][K] (a layer of a stack, offset already applied).
 struct Mat {
@@ -20,7 +20,7 @@ struct Mat {
 };
 
 // Byte offset of layer l of a stack of [N][K] matrices.
-inline Mat mat_layer(Mat m, int l, int N, int K) {
+__host__ __device__ inline Mat mat_layer(Mat m, int l, int N, int K) {
   long long e = (long long)l * N * K;
   if (m.dtype == DT_F32) m.data = (const char*)m.data + e * 4;
   else if (m.dtype == DT_BF16) m.data = (const char*)m.data + e * 2;
@@ -194,10 +194,47 @@ void setup_attn_attributes();
 void setup_draft_attributes();
 
 int num_sms();
+
+// One target pass (prefill or verify) as a single persistent kernel: every
+// phase below runs on all SMs, separated by a grid barrier.
+struct PassDesc {
+  int L, d, nq, nkv, hd, ff, V;
+  float eps, theta;
+  Mat embed, wqkv, wo, wgu, wdown;
+  const float *g_attn, *g_ffn, *g_final;
+  void* pool;
+  long long layer_elems;
+  int n_pages, max_pages;
+  const int32_t* block_table;
+  int32_t *seq_len, *pending;
+  float* hid;
+  int64_t* stats;
+  int B, R, mode;
+  const int32_t* seq_ids;
+  const int32_t* tokens;
+  int32_t *out_tokens, *n_emitted;
+  float* logits;
+  float *x, *qkv, *att, *act, *part_o, *part_ml, *rope_cs;
+  int32_t *pos, *sel_row;
+  unsigned long long* best;
+  unsigned int *counter, *attn_cnt, *tc_cnt, *bar;
+  float* tc_fix;
+  int* err;
+  int* abort_flag;
+  int nsm, n_split, pps;
+  unsigned long long* trace;  // optional [steps][nsm][6] globaltimer marks
+  size_t smem_bytes;          // dynamic shared memory of the launch (set by the launcher)
+  int prefetch;               // pull the next step's weights / pages to L2 before each barrier
+};
+// Launches the persistent pass kernel (cooperative). Returns 1, or -2 when
+// the device cannot hold the whole grid at once (caller uses per-phase
+// kernels), or -1 on a launch error.
+int pass_persistent(const PassDesc& d, cudaStream_t st);
+bool pass_persistent_supported(int hd, int max_rows);
 // tensor-core attention for bf16 caches (head_dim 64 or 128)
 size_t attention_tc_smem(int hd, int qn);
 void setup_attn_tc_attributes();
-int attention_tc_splits(int B, int nkv, int max_pages, int* pps);
+int attention_tc_splits(int B, int nkv, int max_pages, int* pps, int qn);
 int attention_tc(const AttnArgs& a, unsigned int* counters, int pps, cudaStream_t st);
 size_t attention_smem(int hd, int qn);
 

@@ -35,6 +35,8 @@ struct Work {
   unsigned long long* best;
   unsigned int* counter;
   unsigned int* attn_count;
+  unsigned int* bar;
+  int* abort_flag;
   float* tc_fix;
   unsigned int* tc_cnt;
   int* err;
@@ -77,6 +79,8 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
   w.best = b.take<unsigned long long>(base, M);
   w.counter = b.take<unsigned int>(base, 4);
   w.attn_count = b.take<unsigned int>(base, (size_t)B_max * m.n_kv_heads);
+  w.bar = b.take<unsigned int>(base, 4);
+  w.abort_flag = b.take<int>(base, 4);
   w.tc_fix = b.take<float>(base, gemv_tc_fixup_bytes() / sizeof(float));
   w.tc_cnt = b.take<unsigned int>(base, tc_counters(m, d));
   w.err = b.take<int>(base, 4);
@@ -145,6 +149,9 @@ struct spec_ctx {
   Work wk;
   bool graphs = true;
   bool fused_rope = false;
+  bool persistent = false;
+  unsigned long long* trace = nullptr;
+  bool prefetch = true;
   long long launches = 0;
   struct Entry {
     cudaGraphExec_t exec;
@@ -165,7 +172,7 @@ int kv_dt(const spec_ctx* c) { return c->m.kv_dtype == SPEC_F32 ? DT_F32 : DT_BF
 int run_attention(spec_ctx* c, AttnArgs at, cudaStream_t st) {
   if (c->m.kv_dtype == SPEC_BF16 && (c->m.head_dim == 64 || c->m.head_dim == 128)) {
     int pps = 1;
-    at.n_split = attention_tc_splits(at.B, at.nkv, c->kv.max_pages_per_seq, &pps);
+    at.n_split = attention_tc_splits(at.B, at.nkv, c->kv.max_pages_per_seq, &pps, at.R * (at.nq / at.nkv));
     at.pages_per_split = pps;
     return attention_tc(at, c->wk.attn_count, pps, st);
   }
@@ -186,6 +193,27 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     if (r < 0) return -1;   \
     n += r;                 \
   } while (0)
+
+  if (c->persistent && c->fused_rope && pass_persistent_supported(hd, M)) {
+    PassDesc D = {};
+    D.L = m.n_layers; D.d = d; D.nq = nq; D.nkv = nkv; D.hd = hd; D.ff = ff; D.V = m.vocab;
+    D.eps = m.rms_eps; D.theta = m.rope_theta;
+    D.embed = M_(c->w.embed); D.wqkv = M_(c->w.wqkv); D.wo = M_(c->w.wo); D.wgu = M_(c->w.wgu);
+    D.wdown = M_(c->w.wdown); D.g_attn = c->w.g_attn; D.g_ffn = c->w.g_ffn; D.g_final = c->w.g_final;
+    D.pool = c->kv.pool; D.layer_elems = c->layer_elems; D.n_pages = c->kv.n_pages;
+    D.max_pages = c->kv.max_pages_per_seq; D.block_table = c->kv.block_table;
+    D.seq_len = c->state.seq_len; D.pending = c->state.pending; D.hid = c->state.hid; D.stats = c->state.stats;
+    D.B = B; D.R = R; D.mode = mode; D.seq_ids = seq_ids; D.tokens = tokens; D.out_tokens = out_tokens;
+    D.n_emitted = n_emitted; D.logits = logits;
+    D.x = w.x; D.qkv = w.qkv; D.att = w.att; D.act = w.act; D.part_o = w.part_o; D.part_ml = w.part_ml;
+    D.rope_cs = w.rope_cs; D.pos = w.pos; D.sel_row = w.sel_row; D.best = w.best; D.counter = w.counter;
+    D.attn_cnt = w.attn_count; D.tc_cnt = w.tc_cnt; D.bar = w.bar; D.tc_fix = w.tc_fix; D.err = w.err;
+    D.abort_flag = w.abort_flag; D.nsm = num_sms(); D.trace = c->trace; D.prefetch = c->prefetch;
+    D.n_split = attention_tc_splits(B, nkv, c->kv.max_pages_per_seq, &D.pps, R * (nq / nkv));
+    r = pass_persistent(D, st);
+    if (r == -1) return -1;
+    if (r > 0) return r;
+  }
 
   RowsArgs ra = {};
   ra.B = B; ra.R = R; ra.mode = mode; ra.seq_ids = seq_ids; ra.tokens = tokens;
@@ -585,6 +613,13 @@ spec_status spec_sync(spec_ctx* c, void* stream) {
   if (cudaMemcpy(&err, c->wk.err, sizeof err, cudaMemcpyDeviceToHost) != cudaSuccess) return SPEC_ECUDA;
   if (err) {
     if (cudaMemset(c->wk.err, 0, sizeof(int)) != cudaSuccess) return SPEC_ECUDA;
+    if (err == SPEC_ERR_TIMEOUT) {
+      // a bounded wait gave up: reset the barrier state so the next pass can run
+      if (cudaMemset(c->wk.bar, 0, 4 * sizeof(unsigned int)) != cudaSuccess ||
+          cudaMemset(c->wk.abort_flag, 0, sizeof(int)) != cudaSuccess)
+        return SPEC_ECUDA;
+      return SPEC_ETIMEOUT;
+    }
     return err == SPEC_ERR_CAPACITY ? SPEC_ECAPACITY : SPEC_EINVAL;
   }
   return SPEC_OK;
@@ -593,6 +628,19 @@ spec_status spec_sync(spec_ctx* c, void* stream) {
 spec_status spec_set_graphs(spec_ctx* c, int32_t enable) {
   if (!c) return SPEC_EINVAL;
   c->graphs = enable != 0;
+  return SPEC_OK;
+}
+
+spec_status spec_set_option(spec_ctx* c, int32_t option, int64_t value) {
+  if (!c) return SPEC_EINVAL;
+  std::lock_guard<std::mutex> lk(c->mu);
+  if (option == SPEC_OPT_GRAPHS) c->graphs = value != 0;
+  else if (option == SPEC_OPT_PERSISTENT) c->persistent = value != 0;
+  else if (option == SPEC_OPT_TRACE) c->trace = (unsigned long long*)(uintptr_t)value;
+  else if (option == SPEC_OPT_PREFETCH) c->prefetch = value != 0;
+  else return SPEC_EINVAL;
+  for (auto& kv : c->cache) cudaGraphExecDestroy(kv.second.exec);
+  c->cache.clear();
   return SPEC_OK;
 }
 

@@ -37,14 +37,14 @@ def models(request):
     return tw, dw, T, D, prompt, s0
 
 
-def _engine(tw, dw, graphs=True):
+def _engine(tw, dw, graphs=True, persistent=False):
     return binding.Engine(tw, dw, n_slots=2, B_max=2, rows_max=64, max_ctx=CAP, shuffle_pages=True,
-                          graphs=graphs)
+                          graphs=graphs, persistent=persistent)
 
 
-def _prefilled(models, graphs=True):
+def _prefilled(models, graphs=True, persistent=False):
     tw, dw, T, D, prompt, s0 = models
-    eng = _engine(tw, dw, graphs)
+    eng = _engine(tw, dw, graphs, persistent)
     ids = eng.seq_ids([1])
     eng.spec_prefill(ids, eng._in("prompt", prompt.view(1, -1).cuda()))
     eng.sync()
@@ -59,14 +59,16 @@ def test_prefill_matches_oracle(models):
     assert_rows_close(eng.hid[1:2].cpu().numpy(), s0.hid[None], TOL[tw.shape.wdtype], "prefill hidden")
 
 
-@pytest.mark.parametrize("graphs", [True, False])
-def test_verify_logits_and_accept_match_oracle(models, graphs):
+@pytest.mark.parametrize("graphs,persistent", [(True, False), (False, False), (True, True)])
+def test_verify_logits_and_accept_match_oracle(models, graphs, persistent):
+    """Verify pass logits and accepted tokens, per-kernel (with and without
+    graphs) and as one persistent kernel per pass."""
     tw, dw, T, D, prompt, s0 = models
-    eng, ids = _prefilled(models, graphs)
+    eng, ids = _prefilled(models, graphs, persistent)
     eng.close()
     G, _ = oracle.greedy(T, s0.clone(), 8)
     for drafts in ([G[0], G[1], 7], [G[0], G[1], G[2]], [5, 6, 7]):
-        eng2, ids2 = _prefilled(models, graphs)
+        eng2, ids2 = _prefilled(models, graphs, persistent)
         d = eng2._in("drafts", torch.tensor([drafts], dtype=torch.int32).cuda())
         logits = torch.empty((4, W.target.V), dtype=torch.float32, device="cuda")
         out, ne = eng2.spec_verify(ids2, d, logits)
@@ -96,8 +98,9 @@ def test_greedy_decode_matches_oracle(models):
     assert n >= 1
 
 
-@pytest.mark.parametrize("alpha", [0.0, 0.5, 0.8, 1.0])
-def test_speculative_output_equals_greedy(models, alpha):
+@pytest.mark.parametrize("alpha,persistent", [(0.0, False), (0.5, False), (0.8, False), (1.0, False),
+                                              (0.5, True)])
+def test_speculative_output_equals_greedy(models, alpha, persistent):
     """The pages' invariant on the GPU: tokens emitted by speculative steps
     equal plain greedy decoding, bit for bit (same kernels, row results that
     do not depend on the number of verified rows), and the oracle's greedy
@@ -114,7 +117,7 @@ def test_speculative_output_equals_greedy(models, alpha):
     # ref[slot][pos] = token at absolute position pos (pending sits at 64)
     ref[1, 64] = int(s0.pending)
     ref[1, 65:65 + len(greedy)] = torch.tensor(greedy, dtype=torch.int32)
-    eng2, ids2 = _prefilled(models)
+    eng2, ids2 = _prefilled(models, persistent=persistent)
     draws = synth.make_alpha_draws(steps * k, device="cuda")
     offs = synth.make_wrong_offsets(steps * k, W.target.V, device="cuda")
     emitted, per_step = [], []

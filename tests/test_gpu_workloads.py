@@ -20,13 +20,13 @@ from tests.parity import TOL, assert_rows_close, compare_tokens
 pytestmark = pytest.mark.gpu
 
 
-def _setup(w, steps_extra=64):
+def _setup(w, steps_extra=64, persistent=False):
     t = w.target
     tw = synth.make_target(t, device="cuda")
     dw = synth.make_drafter(w.drafter, device="cuda")
     ctx = synth.make_context_lengths(w.B, *w.ctx)
     eng = binding.Engine(tw, dw, n_slots=w.B, B_max=w.B, rows_max=w.k + 1, max_ctx=max(ctx) + steps_extra,
-                         shuffle_pages=True)
+                         shuffle_pages=True, persistent=persistent)
     kvs = []
     for b in range(w.B):
         kv = synth.make_prefilled_kv(t, ctx[b] - 1, device="cuda", seed=synth.SEED_KV + b)
@@ -39,16 +39,17 @@ def _setup(w, steps_extra=64):
     return tw, dw, eng, ids, ctx, kvs, first.cpu()
 
 
-@pytest.mark.parametrize("name,sample", [
-    ("e2b_bf16_b1_ctx2048_k3", [0]),
-    ("e2b_q4_0_b1_ctx4096_k4", [0]),
-    ("e2b_q4_0_b4_ctx4096_k4", [1, 3]),
-    ("e4b_bf16_b8_ragged_k4", [0, 5]),
+@pytest.mark.parametrize("name,sample,persistent", [
+    ("e2b_bf16_b1_ctx2048_k3", [0], False),
+    ("e2b_bf16_b1_ctx2048_k3", [0], True),
+    ("e2b_q4_0_b1_ctx4096_k4", [0], False),
+    ("e2b_q4_0_b4_ctx4096_k4", [1, 3], False),
+    ("e4b_bf16_b8_ragged_k4", [0, 5], False),
 ])
-def test_workload_matches_oracle(name, sample):
+def test_workload_matches_oracle(name, sample, persistent):
     w = configs.WORKLOADS[name]
     t = w.target
-    tw, dw, eng, ids, ctx, kvs, first = _setup(w)
+    tw, dw, eng, ids, ctx, kvs, first = _setup(w, persistent=persistent)
     # GPU: draft, then verify the drafted rows with full logits
     d = eng.spec_draft(ids, w.B, w.k).clone()
     logits = torch.empty((w.B * (w.k + 1), t.V), dtype=torch.float32, device="cuda")
