@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 from speculative_decoding_spec_gb300 import configs, synth  # noqa: E402
 
 PERSISTENT = 0
+DRAFT_CLUSTER = 1
 METRIC = "verify tok/s and HBM GB/s (% of roofline); effective tok/s at set acceptance"
 UNIT = "tok/s"
 
@@ -109,7 +110,8 @@ def setup_workload(w: configs.Workload, steps_total: int, device):
     ctx = synth.make_context_lengths(w.B, *w.ctx)
     grow = steps_total * (w.k + 1) + w.k + 2
     eng = binding.Engine(tw, dw, n_slots=w.B, B_max=w.B, rows_max=w.k + 1, max_ctx=max(ctx) + grow + 64,
-                         shuffle_pages=w.ctx[0] != w.ctx[1], persistent=bool(PERSISTENT))
+                         shuffle_pages=w.ctx[0] != w.ctx[1], persistent=bool(PERSISTENT),
+                         draft_cluster=bool(DRAFT_CLUSTER))
     for b in range(w.B):
         eng.load_prefilled(b, synth.make_prefilled_kv(t, ctx[b] - 1, device=device, seed=synth.SEED_KV + b))
     first = synth.make_tokens(w.B, t.V, device=device).view(w.B, 1)
@@ -304,6 +306,7 @@ def run_gpu(args, w, rank, world):
                      "bytes_per_launch": gb_avg, "ms_per_launch": gms, "traffic": None},
         "gpu_launches": launches,
         "persistent_pass": bool(PERSISTENT),
+        "fused_drafter": bool(DRAFT_CLUSTER),
         "clocks": ck,
     }
     return res, tw, eng, ctx
@@ -364,9 +367,12 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--persistent", type=int, default=0,
                     help="1: one persistent kernel per target pass; 0: one kernel per step")
+    ap.add_argument("--draft-cluster", type=int, default=1,
+                    help="1: all drafter steps in one thread-block-cluster launch; 0: one kernel per operation")
     args = ap.parse_args()
-    global PERSISTENT
+    global PERSISTENT, DRAFT_CLUSTER
     PERSISTENT = args.persistent
+    DRAFT_CLUSTER = args.draft_cluster
     args.warmup = max(args.warmup, 3)
     w = configs.WORKLOADS[args.workload]
 

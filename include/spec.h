@@ -255,12 +255,13 @@ spec_status spec_sync(spec_ctx *ctx, void *stream);
  * for non-NULL streams). */
 spec_status spec_set_graphs(spec_ctx *ctx, int32_t enable);
 
-/* Execution options (for comparisons; both default to 1):
- *  SPEC_OPT_GRAPHS      capture each call shape in a CUDA graph and replay it;
- *  SPEC_OPT_PERSISTENT  run a bf16 target pass of at most 8 rows as one
- *                       persistent kernel (all SMs walk the pass's steps with a
- *                       bounded grid barrier between them) instead of one
- *                       kernel per step;
+/* Execution options (for comparisons):
+ *  SPEC_OPT_GRAPHS      (default 1) capture each call shape in a CUDA graph
+ *                       and replay it;
+ *  SPEC_OPT_PERSISTENT  (default 0) run a bf16 target pass of at most 8 rows
+ *                       as one persistent kernel (all SMs walk the pass's steps
+ *                       with a bounded grid barrier between them) instead of
+ *                       one kernel per step;
  *  SPEC_OPT_TRACE       value = a device pointer to a uint64 buffer of at least
  *                       (3 + 5*n_layers) * n_SMs * 6 entries, or 0: the
  *                       persistent pass records, per step and CTA, the step's
@@ -276,6 +277,19 @@ spec_status spec_set_graphs(spec_ctx *ctx, int32_t enable);
  *                       share of the next step's weights or KV pages towards
  *                       L2 before the grid barrier. */
 #define SPEC_OPT_PREFETCH 4
+/*  SPEC_OPT_DRAFT_CLUSTER (default 1) run all k drafter steps as one launch of
+ *                       one thread-block cluster per sequence (weights
+ *                       streamed through shared memory by bulk copies,
+ *                       activations exchanged through distributed shared
+ *                       memory); 0, or shapes it does not cover, run one
+ *                       kernel per drafter operation. */
+#define SPEC_OPT_DRAFT_CLUSTER 5
+/*  SPEC_OPT_DRAFT_TRACE value = a device pointer to a uint64 buffer of at least
+ *                       1 + k * (7 + 10 * n_drafter_layers) entries, or 0: the
+ *                       fused drafter records, for sequence 0, globaltimer
+ *                       stamps (ns) at its start, after each operation's last
+ *                       weight chunk and after each cluster barrier. */
+#define SPEC_OPT_DRAFT_TRACE 6
 spec_status spec_set_option(spec_ctx *ctx, int32_t option, int64_t value);
 
 /* Number of kernels the library launched (or replayed inside graphs) since the

@@ -23,7 +23,8 @@ EXPORTS = ["spec_workspace_bytes", "spec_init", "spec_prefill", "spec_draft", "s
            "spec_decode", "spec_inject_drafts", "spec_stats", "spec_sync", "spec_set_graphs",
            "spec_kernel_launches", "spec_status_str", "spec_destroy", "spec_linear",
            "spec_linear_workspace_bytes", "spec_linear_noalloc", "spec_set_option"]
-SPEC_OPT_GRAPHS, SPEC_OPT_PERSISTENT, SPEC_OPT_TRACE, SPEC_OPT_PREFETCH = 1, 2, 3, 4
+(SPEC_OPT_GRAPHS, SPEC_OPT_PERSISTENT, SPEC_OPT_TRACE, SPEC_OPT_PREFETCH, SPEC_OPT_DRAFT_CLUSTER,
+ SPEC_OPT_DRAFT_TRACE) = 1, 2, 3, 4, 5, 6
 SPEC_LINEAR_NOALLOC_MAX_ROWS = 523776
 
 
@@ -204,7 +205,8 @@ class Engine:
     around one spec_ctx and forwards calls to the C ABI on its own stream."""
 
     def __init__(self, tw, dw=None, n_slots=1, B_max=1, rows_max=4, max_ctx=256, shuffle_pages=False,
-                 device="cuda", graphs=True, persistent=False):
+                 device="cuda", graphs=True, persistent=False,
+                 draft_cluster=True):
         L = lib()
         t = tw.shape
         self.tw, self.dw, self.shape = tw, dw, t
@@ -251,6 +253,7 @@ class Engine:
         if not graphs:
             check("spec_set_graphs", L.spec_set_graphs(ctx, 0))
         check("spec_set_option", L.spec_set_option(ctx, SPEC_OPT_PERSISTENT, int(bool(persistent))))
+        check("spec_set_option", L.spec_set_option(ctx, SPEC_OPT_DRAFT_CLUSTER, int(bool(draft_cluster))))
         self._bufs = {}
 
     # -- helpers ------------------------------------------------------------

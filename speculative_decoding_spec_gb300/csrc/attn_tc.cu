@@ -33,6 +33,15 @@ size_t attention_tc_smem(int hd, int qn) {
   return (size_t)2 * qt * 16 * st * 2 + std::max(std::max(pages, combine), qstage);
 }
 
+// Shared memory of a CTA running the attention with `pw` page slots.
+size_t attention_tc_smem_slots(int hd, int qn, int pw) {
+  const int qt = host_qt(qn), st = hd + 8, kg = qt == 1 ? 4 : 1;
+  const size_t pages = (size_t)2 * pw * PAGE * st * 2;
+  const size_t combine = (size_t)qt * kg * pw * 16 * (hd + 2) * 4 + (size_t)qt * 16 * 4;
+  const size_t qstage = (size_t)(qn + 16) * hd * 4;
+  return (size_t)2 * qt * 16 * st * 2 + std::max(std::max(pages, combine), qstage);
+}
+
 void setup_attn_tc_attributes() {
   cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);

@@ -30,6 +30,7 @@ namespace spec {
 namespace atc {
 
 constexpr int PAGE = 64;
+constexpr int PGS_MAX = 256;  // page ids of a split cached in shared memory
 
 static SPEC_DEV void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                        uint32_t b1) {
@@ -207,13 +208,16 @@ struct AttnTc {
   // bx = sequence * n_kv + KV head, by = split (of a.n_split); the split covers
   // pages [by*pps, (by+1)*pps), pps a multiple of the page slots. standalone:
   // own launch (PDL waits) rather than a step of the persistent pass kernel.
+  // pw_cap > 0 caps the page slots (and so the shared memory) below what the
+  // CTA's warps could fill.
   static SPEC_DEV void run(const AttnArgs& a, int pps, unsigned int* counters, unsigned char* smem, int bx,
-                           int by, bool standalone, size_t smem_bytes) {
+                           int by, bool standalone, size_t smem_bytes, int pw_cap = 0) {
     const int b = bx / a.nkv, kvh = bx % a.nkv, split = by;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
     const int NW = blockDim.x >> 5;
     const int G = a.nq / a.nkv, QN = a.R * G, QT = (QN + 15) / 16;
-    const int KG = key_groups(QT), PW = page_slots(QT, NW);
+    const int KG = key_groups(QT);
+    const int PW = pw_cap > 0 && page_slots(QT, NW) > pw_cap ? pw_cap : page_slots(QT, NW);
     const int qt = warp % QT, rest = warp / QT, kg = rest % KG, pslot = rest / KG;
     const bool active = warp < QT * KG * PW;
     __nv_bfloat16* Qh = reinterpret_cast<__nv_bfloat16*>(smem);
@@ -233,11 +237,19 @@ struct AttnTc {
       grid_dep_wait();
       grid_dep_launch();
     }
-    bool pages_ok = true;
-    for (int p = p0; p < p1; ++p) {
+    // the split's page ids, read once in parallel (and checked) when they fit
+    __shared__ int s_pgs[PGS_MAX];
+    __shared__ int s_bad;
+    const bool ids_cached = p1 - p0 <= PGS_MAX;
+    if (threadIdx.x == 0) s_bad = 0;
+    __syncthreads();
+    for (int p = p0 + (int)threadIdx.x; p < p1; p += blockDim.x) {
       const int pg = a.block_table[(size_t)slot * a.max_pages + p];
-      if (pg < 0 || pg >= a.n_pages) pages_ok = false;
+      if (pg < 0 || pg >= a.n_pages) s_bad = 1;
+      if (ids_cached) s_pgs[p - p0] = pg;
     }
+    __syncthreads();
+    const bool pages_ok = s_bad == 0;
     if (!pages_ok && threadIdx.x == 0) set_error(a.err, SPEC_ERR_CAPACITY);
     const int pend = pages_ok ? p1 : p0;
 
@@ -304,7 +316,9 @@ struct AttnTc {
       const int nr = min(PW, pend - rb);
       __syncthreads();
       // page ids first: a copy must not wait for its own table lookup
-      if ((int)threadIdx.x < nr) s_pg[threadIdx.x] = a.block_table[(size_t)slot * a.max_pages + rb + threadIdx.x];
+      if ((int)threadIdx.x < nr)
+        s_pg[threadIdx.x] =
+            ids_cached ? s_pgs[rb - p0 + threadIdx.x] : a.block_table[(size_t)slot * a.max_pages + rb + threadIdx.x];
       __syncthreads();
       constexpr int CPR = HD / 8;
       for (int t = threadIdx.x; t < nr * PAGE * CPR; t += blockDim.x) {
@@ -341,8 +355,8 @@ struct AttnTc {
 
     // combine the warps of each query tile (shared memory, fixed warp order)
     constexpr int RS = HD + 2;  // o[HD], m, l per row
-    float* scr = reinterpret_cast<float*>(Kb);  // [NW][16][RS]
-    float* mrow = scr + (size_t)NW * 16 * RS;     // [QT*16] combined max per query row
+    float* scr = reinterpret_cast<float*>(Kb);  // [active warps][16][RS]
+    float* mrow = scr + (size_t)QT * KG * PW * 16 * RS;  // [QT*16] combined max per query row
     if (active) {
       float* w0 = scr + ((size_t)warp * 16 + g) * RS;
       float* w1 = w0 + 8 * RS;

@@ -180,6 +180,53 @@ struct ClusterArgs {
 };
 int cluster_head(const ClusterArgs& a, cudaStream_t st);
 
+// All k drafter steps of B sequences in one launch: one thread-block cluster
+// per sequence (draft_cluster.cu). The host fills the model, state and buffer
+// fields; draft_cluster_plan() fills the layout fields (ncta .. off_y).
+struct DraftDesc {
+  int B, k;
+  int d, h, L, dnq, nkv, hd, ff;      // target width; drafter width, layers, q heads, kv heads, ffn
+  int V, C, top_c, cs, clustered;     // vocabulary; centroids, clusters kept, cluster size
+  float eps, theta;
+  int wdtype, kv_dtype;
+  Mat embed;                          // target embedding [V][d]
+  Mat w_in, wq, wo, wgu, wdown, w_out, centroids, vocab;
+  const float *g_in_h, *g_in_e, *g_attn, *g_ffn, *g_out;
+  const int32_t* perm;                // [V] vocabulary row -> token id (clustered head)
+  const int32_t* seq_ids;             // [B]
+  const int32_t* seq_len;             // state [slots]
+  const int32_t* pending;             // state [slots]
+  const float* hid;                   // state [slots][d]
+  const void* pool;                   // KV pool
+  long long layer_off;                // elements to the target's last layer
+  int n_pages, max_pages;
+  const int32_t* block_table;         // [slots][max_pages]
+  float* part;                        // attention partials, part_stride floats per sequence (fp32 cache)
+  long long part_stride;
+  // tensor-core attention (bf16 cache): queries and RoPE rows in, output out
+  float* q;                           // [B][dnq*hd]
+  float* rope;                        // [B][hd]
+  float* att;                         // [B][dnq*hd]
+  float* part_o;                      // [B][dnq][ncta][hd] split partials
+  float* part_ml;                     // [B][dnq][ncta][2]
+  unsigned int* att_cnt;              // [B][nkv] arrival counters, zero between launches
+  long long layer_elems;              // pool elements per target layer
+  int tlayer;                         // the target's last layer
+  int32_t* drafts;                    // out [B][k]
+  int* err;
+  unsigned long long* trace;          // optional phase timestamps (sequence 0, CTA 0)
+  // layout (draft_cluster_plan)
+  int ncta, ns, pw_cap;
+  int off_u1, off_qaa, off_u, off_sc, off_part, off_y;
+  size_t smem;
+};
+// Fills the layout fields; false when the shapes are outside what the fused
+// drafter handles (the caller then runs the per-kernel drafter).
+bool draft_cluster_plan(DraftDesc& d);
+// Attention partial floats per sequence (any plan), G = q heads per kv head.
+long long draft_cluster_part_floats(int G, int hd);
+int draft_cluster(const DraftDesc& d, cudaStream_t st);
+
 int inject_drafts(int B, int k, const int32_t* seq_ids, const int32_t* seq_len, int32_t* drafts,
                   const int32_t* ref, int ref_len, float alpha, const float* draws,
                   const int32_t* offsets, int vocab, int* err, cudaStream_t st);
@@ -233,6 +280,7 @@ int pass_persistent(const PassDesc& d, cudaStream_t st);
 bool pass_persistent_supported(int hd, int max_rows);
 // tensor-core attention for bf16 caches (head_dim 64 or 128)
 size_t attention_tc_smem(int hd, int qn);
+size_t attention_tc_smem_slots(int hd, int qn, int pw);
 void setup_attn_tc_attributes();
 int attention_tc_splits(int B, int nkv, int max_pages, int* pps, int qn);
 int attention_tc(const AttnArgs& a, unsigned int* counters, int pps, cudaStream_t st);

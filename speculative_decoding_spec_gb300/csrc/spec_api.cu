@@ -42,6 +42,9 @@ struct Work {
   int* err;
   // drafter
   float *d_cat, *d_u, *d_q, *d_att, *d_act, *d_h, *d_scores, *d_rope, *d_part_o, *d_part_ml;
+  float* d_cpart;           // fused drafter: attention partials (fp32 cache)
+  float *d_cpo, *d_cpml;    // fused drafter: tensor-core attention split partials
+  unsigned int* d_ccnt;     // fused drafter: attention arrival counters
   int32_t *d_chosen, *d_drafts;
   unsigned long long* d_best;
   unsigned int* d_counter;
@@ -100,6 +103,11 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
     w.d_drafts = b.take<int32_t>(base, (size_t)B_max * KMAX);
     w.d_best = b.take<unsigned long long>(base, B_max);
     w.d_counter = b.take<unsigned int>(base, 4);
+    w.d_cpart = b.take<float>(base, (size_t)B_max *
+                                        draft_cluster_part_floats(d->n_q_heads / m.n_kv_heads, m.head_dim));
+    w.d_cpo = b.take<float>(base, (size_t)B_max * d->n_q_heads * 16 * m.head_dim);
+    w.d_cpml = b.take<float>(base, (size_t)B_max * d->n_q_heads * 16 * 2);
+    w.d_ccnt = b.take<unsigned int>(base, (size_t)B_max * m.n_kv_heads);
   }
   w.bytes = (b.off + 255) & ~size_t(255);
   return w;
@@ -152,6 +160,10 @@ struct spec_ctx {
   bool persistent = false;
   unsigned long long* trace = nullptr;
   bool prefetch = true;
+  bool draft_cluster = true;
+  unsigned long long* dtrace = nullptr;
+  int cluster_plan = 0;     // fused drafter layout: 0 not made yet, 1 made, -1 not supported
+  DraftDesc cplan;
   long long launches = 0;
   struct Entry {
     cudaGraphExec_t exec;
@@ -292,6 +304,45 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
 }
 
 // ---- the drafter: k autoregressive steps on the target's last hidden state ---
+// The fused drafter's description for this context (layout planned once).
+bool cluster_desc(spec_ctx* c, DraftDesc& D) {
+  if (c->cluster_plan == 0) {
+    const spec_model_desc& m = c->m;
+    const spec_drafter_desc& dd = c->dd;
+    const spec_drafter_weights& dw = c->dw;
+    DraftDesc P = {};
+    P.B = 1; P.k = 1;
+    P.d = m.d_model; P.h = dd.hidden; P.L = dd.n_layers; P.dnq = dd.n_q_heads; P.nkv = m.n_kv_heads;
+    P.hd = m.head_dim; P.ff = dd.d_ff; P.V = m.vocab; P.clustered = dd.clustered;
+    P.C = dd.clustered ? dd.n_centroids : 0; P.top_c = dd.top_c;
+    P.cs = dd.clustered ? m.vocab / dd.n_centroids : 0;
+    P.eps = m.rms_eps; P.theta = m.rope_theta; P.wdtype = dd.w_dtype; P.kv_dtype = kv_dt(c);
+    P.embed = M_(c->w.embed);
+    P.w_in = M_(dw.w_in); P.wq = M_(dw.wq); P.wo = M_(dw.wo); P.wgu = M_(dw.wgu); P.wdown = M_(dw.wdown);
+    P.w_out = M_(dw.w_out); P.centroids = M_(dw.centroids); P.vocab = M_(dw.vocab);
+    P.g_in_h = dw.g_in_h; P.g_in_e = dw.g_in_e; P.g_attn = dw.g_attn; P.g_ffn = dw.g_ffn; P.g_out = dw.g_out;
+    P.perm = dw.perm;
+    P.seq_len = c->state.seq_len; P.pending = c->state.pending; P.hid = c->state.hid;
+    P.pool = c->kv.pool; P.layer_off = (long long)(m.n_layers - 1) * c->layer_elems;
+    P.n_pages = c->kv.n_pages; P.max_pages = c->kv.max_pages_per_seq; P.block_table = c->kv.block_table;
+    P.part = c->wk.d_cpart; P.err = c->wk.err;
+    P.q = c->wk.d_q; P.rope = c->wk.d_rope; P.att = c->wk.d_att; P.part_o = c->wk.d_cpo;
+    P.part_ml = c->wk.d_cpml; P.att_cnt = c->wk.d_ccnt; P.layer_elems = c->layer_elems;
+    P.tlayer = m.n_layers - 1;
+    // every matrix the bulk copies read must start 16-byte aligned
+    bool aligned = true;
+    for (const spec_matrix* mm : {&dw.w_in, &dw.wq, &dw.wo, &dw.wgu, &dw.wdown, &dw.w_out, &dw.vocab})
+      aligned = aligned && ((uintptr_t)mm->data % 16 == 0) && ((uintptr_t)mm->scales % 16 == 0);
+    if (dd.clustered)
+      aligned = aligned && ((uintptr_t)dw.centroids.data % 16 == 0) && ((uintptr_t)dw.centroids.scales % 16 == 0);
+    c->cluster_plan = aligned && draft_cluster_plan(P) ? 1 : -1;
+    c->cplan = P;
+  }
+  if (c->cluster_plan != 1) return false;
+  D = c->cplan;
+  return true;
+}
+
 int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* drafts, cudaStream_t st) {
   const spec_model_desc& m = c->m;
   const spec_drafter_desc& dd = c->dd;
@@ -299,6 +350,11 @@ int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* dr
   const Work& w = c->wk;
   const int d = m.d_model, h = dd.hidden, hd = m.head_dim, dq = dd.n_q_heads * hd, ff = dd.d_ff;
   int n = 0, r;
+  DraftDesc D;
+  if (c->draft_cluster && cluster_desc(c, D)) {
+    D.B = B; D.k = k; D.seq_ids = seq_ids; D.drafts = drafts; D.trace = c->dtrace;
+    return draft_cluster(D, st);
+  }
   for (int j = 1; j <= k; ++j) {
     DraftInArgs di = {};
     di.B = B; di.j = j; di.k = k; di.d = d; di.hd = hd; di.seq_ids = seq_ids;
@@ -507,6 +563,12 @@ spec_status spec_init(const spec_model_desc* model, const spec_weights* weights,
     delete c;
     return SPEC_ECUDA;
   }
+  if (c->has_drafter) {
+    // lay out the fused drafter now: planning queries the device, which a
+    // stream capture in progress must not see
+    DraftDesc D;
+    cluster_desc(c, D);
+  }
   *out = c;
   return SPEC_OK;
 }
@@ -638,6 +700,8 @@ spec_status spec_set_option(spec_ctx* c, int32_t option, int64_t value) {
   else if (option == SPEC_OPT_PERSISTENT) c->persistent = value != 0;
   else if (option == SPEC_OPT_TRACE) c->trace = (unsigned long long*)(uintptr_t)value;
   else if (option == SPEC_OPT_PREFETCH) c->prefetch = value != 0;
+  else if (option == SPEC_OPT_DRAFT_CLUSTER) c->draft_cluster = value != 0;
+  else if (option == SPEC_OPT_DRAFT_TRACE) c->dtrace = (unsigned long long*)(uintptr_t)value;
   else return SPEC_EINVAL;
   for (auto& kv : c->cache) cudaGraphExecDestroy(kv.second.exec);
   c->cache.clear();

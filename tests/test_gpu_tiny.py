@@ -37,14 +37,14 @@ def models(request):
     return tw, dw, T, D, prompt, s0
 
 
-def _engine(tw, dw, graphs=True, persistent=False):
+def _engine(tw, dw, graphs=True, persistent=False, draft_cluster=True):
     return binding.Engine(tw, dw, n_slots=2, B_max=2, rows_max=64, max_ctx=CAP, shuffle_pages=True,
-                          graphs=graphs, persistent=persistent)
+                          graphs=graphs, persistent=persistent, draft_cluster=draft_cluster)
 
 
-def _prefilled(models, graphs=True, persistent=False):
+def _prefilled(models, graphs=True, persistent=False, draft_cluster=True):
     tw, dw, T, D, prompt, s0 = models
-    eng = _engine(tw, dw, graphs, persistent)
+    eng = _engine(tw, dw, graphs, persistent, draft_cluster)
     ids = eng.seq_ids([1])
     eng.spec_prefill(ids, eng._in("prompt", prompt.view(1, -1).cuda()))
     eng.sync()
@@ -144,13 +144,32 @@ def test_speculative_output_equals_greedy(models, alpha, persistent):
     assert st.accepted == st.emitted - st.passes and st.drafted == steps * k
 
 
-def test_drafter_matches_oracle(models):
+@pytest.mark.parametrize("draft_cluster", [True, False])
+def test_drafter_matches_oracle(models, draft_cluster):
+    """The k drafted tokens, from the fused one-cluster drafter and from the
+    one-kernel-per-operation drafter."""
     tw, dw, T, D, prompt, s0 = models
-    eng, ids = _prefilled(models)
+    eng, ids = _prefilled(models, draft_cluster=draft_cluster)
     d = eng.spec_draft(ids, 1, W.k)
     eng.sync()
     ref, mg = oracle.draft(T, D, s0.clone(), W.k)
     compare_tokens(d[0].cpu().numpy(), ref, mg)
+
+
+def test_fused_drafter_is_one_launch(models):
+    """With fp32 or bf16 weights the tiny drafter runs as one kernel launch per
+    draft call (Q4_0 needs every reduction width to be a multiple of 256 and
+    falls back to the per-operation kernels at width 64)."""
+    tw, dw, T, D, prompt, s0 = models
+    eng, ids = _prefilled(models, graphs=False)
+    before = eng.kernel_launches()
+    eng.spec_draft(ids, 1, W.k)
+    eng.sync()
+    n = eng.kernel_launches() - before
+    if tw.shape.wdtype == configs.Q4_0:
+        assert n > 1
+    else:
+        assert n == 1
 
 
 def test_step_emits_greedy_tokens(models):

@@ -20,13 +20,14 @@ from tests.parity import TOL, assert_rows_close, compare_tokens
 pytestmark = pytest.mark.gpu
 
 
-def _setup(w, steps_extra=64, persistent=False):
+def _setup(w, steps_extra=64, persistent=False, draft_cluster=True):
     t = w.target
     tw = synth.make_target(t, device="cuda")
     dw = synth.make_drafter(w.drafter, device="cuda")
     ctx = synth.make_context_lengths(w.B, *w.ctx)
     eng = binding.Engine(tw, dw, n_slots=w.B, B_max=w.B, rows_max=w.k + 1, max_ctx=max(ctx) + steps_extra,
-                         shuffle_pages=True, persistent=persistent)
+                         shuffle_pages=True, persistent=persistent,
+                         draft_cluster=draft_cluster)
     kvs = []
     for b in range(w.B):
         kv = synth.make_prefilled_kv(t, ctx[b] - 1, device="cuda", seed=synth.SEED_KV + b)
@@ -39,17 +40,18 @@ def _setup(w, steps_extra=64, persistent=False):
     return tw, dw, eng, ids, ctx, kvs, first.cpu()
 
 
-@pytest.mark.parametrize("name,sample,persistent", [
-    ("e2b_bf16_b1_ctx2048_k3", [0], False),
-    ("e2b_bf16_b1_ctx2048_k3", [0], True),
-    ("e2b_q4_0_b1_ctx4096_k4", [0], False),
-    ("e2b_q4_0_b4_ctx4096_k4", [1, 3], False),
-    ("e4b_bf16_b8_ragged_k4", [0, 5], False),
+@pytest.mark.parametrize("name,sample,persistent,draft_cluster", [
+    ("e2b_bf16_b1_ctx2048_k3", [0], False, True),
+    ("e2b_bf16_b1_ctx2048_k3", [0], True, False),
+    ("e2b_q4_0_b1_ctx4096_k4", [0], False, True),
+    ("e2b_q4_0_b4_ctx4096_k4", [1, 3], False, True),
+    ("e2b_q4_0_b4_ctx4096_k4", [2], False, False),
+    ("e4b_bf16_b8_ragged_k4", [0, 5], False, True),
 ])
-def test_workload_matches_oracle(name, sample, persistent):
+def test_workload_matches_oracle(name, sample, persistent, draft_cluster):
     w = configs.WORKLOADS[name]
     t = w.target
-    tw, dw, eng, ids, ctx, kvs, first = _setup(w, persistent=persistent)
+    tw, dw, eng, ids, ctx, kvs, first = _setup(w, persistent=persistent, draft_cluster=draft_cluster)
     # GPU: draft, then verify the drafted rows with full logits
     d = eng.spec_draft(ids, w.B, w.k).clone()
     logits = torch.empty((w.B * (w.k + 1), t.V), dtype=torch.float32, device="cuda")
