@@ -273,9 +273,10 @@ spec_status spec_set_graphs(spec_ctx *ctx, int32_t enable);
 #define SPEC_OPT_GRAPHS 1
 #define SPEC_OPT_PERSISTENT 2
 #define SPEC_OPT_TRACE 3
-/*  SPEC_OPT_PREFETCH    (default 1) in the persistent pass, each CTA pulls its
- *                       share of the next step's weights or KV pages towards
- *                       L2 before the grid barrier. */
+/*  SPEC_OPT_PREFETCH    (default 0) each projection CTA first pulls its share
+ *                       of the weights towards L2 (bulk L2 prefetch); in the
+ *                       persistent pass, of the next step's weights or KV
+ *                       pages before the grid barrier. */
 #define SPEC_OPT_PREFETCH 4
 /*  SPEC_OPT_DRAFT_CLUSTER (default 1) run all k drafter steps as one launch of
  *                       one thread-block cluster per sequence (weights

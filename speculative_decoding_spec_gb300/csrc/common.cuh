@@ -89,6 +89,11 @@ SPEC_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents
 
 // Prefetch one 128-byte line into L2 (no register or shared-memory cost).
 SPEC_DEV void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+// Prefetch a contiguous range into L2 with one bulk (TMA) request; p 16-byte
+// aligned, bytes a multiple of 16.
+SPEC_DEV void prefetch_l2_bulk(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // 128-bit streaming load of weights: read once, do not keep in L1.
 SPEC_DEV uint4 ldg_stream(const void* p) {

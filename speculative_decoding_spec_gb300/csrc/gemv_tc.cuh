@@ -20,10 +20,10 @@
 // product of the exact bf16 weights. Each row's result depends only on that
 // row and X, never on M.
 //
-// Work split. Persistent CTAs of 16 warps; CTA c owns a balanced range of row
-// tiles. When a CTA has fewer tiles than warps, K is cut into slices and the
-// slice partials are added in a fixed order; when X does not fit in shared
-// memory, K is staged in chunks (each chunk a further set of slices).
+// Work split. One CTA of 16 warps per SM; CTA c owns a balanced range of
+// whole 16-row tiles (no tile is shared between CTAs), and its warps split the
+// CTA's (tile, 128-column chunk) units evenly; a tile cut between warps is
+// summed in shared memory in chunk order.
 #pragma once
 #include <stdint.h>
 
@@ -70,7 +70,12 @@ static SPEC_DEV uint32_t bf16x2(float lo, float hi) {
 }
 
 // first unit of CTA b
-__device__ HOSTDEV_INLINE int unit_begin(int b, const SkPlan& p) { return (int)(((long long)b * p.U) / p.grid); }
+// First unit of CTA b: every CTA owns whole 16-row tiles (the tile counts of
+// two CTAs differ by at most one), so no tile is split between CTAs and no
+// cross-CTA partial sums are needed; the warps of a CTA split its units.
+__device__ HOSTDEV_INLINE int unit_begin(int b, const SkPlan& p) {
+  return (int)(((long long)b * p.T) / p.grid) * p.C;
+}
 
 template <int TW>
 struct Sk {
@@ -126,20 +131,23 @@ struct Sk {
     }
   }
 
-  // prefetch.global.L2 of the weight lines of units [u0, u1), at most 256 KB
+  // L2 prefetch of the weight rows of units [u0, u1), at most 512 KB: one
+  // bulk prefetch (cp.async.bulk.prefetch.L2) per row segment, so issuing it
+  // costs a few instructions per tile rather than one per 128-byte line.
   SPEC_DEV void prefetch_slice(int u0, int u1) const {
-    const int per_unit = 32;  // 16 rows x 2 lines of 128 B (a unit is 128 columns)
-    const int n = min((u1 - u0) * per_unit, 2048);
+    if (u1 <= u0) return;
+    const int t0 = u0 / p.C, t1 = (u1 - 1) / p.C;
+    const int max_tiles = max(1, (512 << 10) / (16 * a.K * 2));
+    const int nt = min(t1 - t0 + 1, max_tiles);
     const __nv_bfloat16* W = (const __nv_bfloat16*)a.W.data;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) {
-      const int u = u0 + i / per_unit, r = (i % per_unit) >> 1, half = i & 1;
-      const int t = u / p.C, ch = u - t * p.C;
-      const int g = r & 7;
+    for (int i = threadIdx.x; i < nt * 16; i += blockDim.x) {
+      const int t = t0 + (i >> 4), r = i & 15, g = r & 7;
       const bool hi_row = r >= 8;
       if (!(hi_row ? ok_g8(t, g) : ok_g(t, g))) continue;
       const int row = hi_row ? row_g8(t, g) : row_g(t, g);
-      const int col = ch * KCH + half * 64;
-      if (col < a.K) prefetch_l2(W + (size_t)row * a.K + col);
+      const int cs = t == t0 ? u0 - t0 * p.C : 0, ce = t == t1 ? u1 - t1 * p.C : p.C;
+      const int col0 = cs * KCH, col1 = min(a.K, ce * KCH);
+      if (col1 > col0) prefetch_l2_bulk(W + (size_t)row * a.K + col0, (unsigned)(col1 - col0) * 2);
     }
   }
 
@@ -322,7 +330,7 @@ struct Sk {
     // towards L2 (capped) and put the first unit in flight before the wait
     uint4 wa[4], wb[4];
     if (standalone) {
-      prefetch_slice(u0, u1);
+      if (a.prefetch) prefetch_slice(u0, u1);
       if (wa_ < wb_) load_unit(wa_, wa, wb);
       grid_dep_wait();
       grid_dep_launch();
@@ -464,14 +472,14 @@ __host__ __device__ inline int map_of(int epi) {
   return epi == EPI_GEGLU ? MAP_PAIR : epi == EPI_ROPE ? MAP_ROPE : MAP_PLAIN;
 }
 
-// Stream-K plan: T tiles x C chunks spread over min(U, nsm) CTAs of TW warps.
+// Plan: T tiles x C chunks over min(T, nsm) CTAs of TW warps.
 template <int TW = 16>
 __host__ __device__ inline SkPlan plan(const GemvArgs& a, int map, int nsm) {
   SkPlan p;
   p.T = map == MAP_PAIR ? (a.geglu_half + 7) / 8 : map == MAP_ROPE ? a.N / 16 : (a.N + 15) / 16;
   p.C = (a.K + KCH - 1) / KCH;
   p.U = p.T * p.C;
-  p.grid = p.U < nsm ? p.U : nsm;
+  p.grid = p.T < nsm ? p.T : nsm;
   p.Ms = a.M;
   p.xs = a.K + XPAD;
   const size_t xb = (size_t)(p.Ms > 1 ? p.Ms : 1) * p.xs * 2 * 2;

@@ -86,6 +86,7 @@ struct GemvArgs {
   float* tc_fix;            // tensor-core kernel: split-tile partials (gemv_tc_fixup_bytes())
   unsigned int* tc_cnt;     // tensor-core kernel: per-tile arrival counters, zero between launches
   int pdl;                  // launch with programmatic dependent launch
+  int prefetch;             // tensor-core kernel: pull the CTA's weight slice to L2 first
 };
 int gemv(const GemvArgs& a, cudaStream_t st);
 

@@ -77,7 +77,7 @@ extern "C" spec_status spec_linear_noalloc(const spec_matrix* w, int32_t N, int3
   g.X = x; g.ldx = K; g.M = M; g.N = N; g.K = K;
   g.W = spec::Mat{w->dtype, w->data, w->scales};
   g.gain = gain; g.eps = eps;
-  g.epi = spec::EPI_STORE; g.Y = y; g.ldy = N; g.pdl = 0;
+  g.epi = spec::EPI_STORE; g.Y = y; g.ldy = N; g.pdl = 0; g.prefetch = 0;
   g.tc_fix = (float*)base;
   g.tc_cnt = cnt;
   if (spec::gemv(g, st) < 0) return SPEC_ECUDA;

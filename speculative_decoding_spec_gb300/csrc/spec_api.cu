@@ -159,7 +159,7 @@ struct spec_ctx {
   bool fused_rope = false;
   bool persistent = false;
   unsigned long long* trace = nullptr;
-  bool prefetch = true;
+  bool prefetch = false;
   bool draft_cluster = true;
   unsigned long long* dtrace = nullptr;
   int cluster_plan = 0;     // fused drafter layout: 0 not made yet, 1 made, -1 not supported
@@ -439,6 +439,7 @@ int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* dr
 int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st) {
   g.tc_fix = c->wk.tc_fix;
   g.tc_cnt = c->wk.tc_cnt;
+  g.prefetch = c->prefetch ? 1 : 0;
   return gemv(g, st);
 }
 
@@ -643,7 +644,7 @@ spec_status spec_linear(const spec_matrix* w, int32_t N, int32_t K, const float*
   if (!workspace || ws_bytes < spec_linear_workspace_bytes(N, K, M)) return SPEC_ECAPACITY;
   GemvArgs g = {};
   g.X = x; g.ldx = K; g.M = M; g.N = N; g.K = K; g.W = M_(*w); g.gain = gain; g.eps = eps;
-  g.epi = EPI_STORE; g.Y = y; g.ldy = N; g.pdl = 0;
+  g.epi = EPI_STORE; g.Y = y; g.ldy = N; g.pdl = 0; g.prefetch = 0;
   g.tc_fix = (float*)workspace;
   g.tc_cnt = (unsigned int*)((char*)workspace + gemv_tc_fixup_bytes());
   static std::once_flag once;

@@ -1,0 +1,79 @@
+"""Small, self-contained GPU cases for profiling the hot kernels with ncu.
+
+    python -m speculative_decoding_spec_gb300.profile_cases projections
+        every projection of one verify pass of the E2B-shaped bf16 target
+        (24 layers x QKV, O, gate/up, down, then the LM head; M = 4 rows),
+        run twice -- the launch sequence whose average the bench's roofline
+        line reports. About 2.5 GB of weights, so nothing stays in L2.
+    python -m speculative_decoding_spec_gb300.profile_cases draft
+        three calls of the fused drafter (k = 3) on the E2B-shaped workload.
+    python -m speculative_decoding_spec_gb300.profile_cases verify
+        three verify passes (k = 3) of the E2B-shaped workload.
+
+Inputs are the seeded synthetic weights and caches of the workload; nothing
+here checks results (the tests do).
+"""
+import sys
+
+import torch
+
+from . import binding, configs, synth
+
+WORKLOAD = "e2b_bf16_b1_ctx2048_k3"
+
+
+def _engine(w):
+    t = w.target
+    tw = synth.make_target(t, device="cuda")
+    dw = synth.make_drafter(w.drafter, device="cuda")
+    ctx = synth.make_context_lengths(w.B, *w.ctx)
+    eng = binding.Engine(tw, dw, n_slots=w.B, B_max=w.B, rows_max=w.k + 1, max_ctx=max(ctx) + 64)
+    for b in range(w.B):
+        eng.load_prefilled(b, synth.make_prefilled_kv(t, ctx[b] - 1, device="cuda", seed=synth.SEED_KV + b))
+    ids = eng.seq_ids(list(range(w.B)))
+    eng.spec_prefill(ids, eng._in("first", synth.make_tokens(w.B, t.V, device="cuda").view(w.B, 1)))
+    eng.sync()
+    return tw, eng, ids
+
+
+def projections(w):
+    t = w.target
+    tw = synth.make_target(t, device="cuda")
+    shapes = [(tw.wqkv, t.d), (tw.wo, t.nq * t.hd), (tw.wgu, t.d), (tw.wdown, t.ff)]
+    seq = [(W, K, l) for l in range(t.L) for W, K in shapes] + [(tw.embed, t.d, 0)]
+    xs = {K: torch.randn((w.M, K), device="cuda") for K in {t.d, t.nq * t.hd, t.ff}}
+    ys = {id(W): torch.empty((w.M, W.N), device="cuda") for W, _, _ in seq}
+    for _ in range(2):
+        for W, K, l in seq:
+            binding.spec_linear(W, xs[K], layer=l, y=ys[id(W)])
+        torch.cuda.synchronize()
+
+
+def draft(w):
+    _, eng, ids = _engine(w)
+    for _ in range(3):
+        eng.spec_draft(ids, w.B, w.k)
+    eng.sync()
+
+
+def verify(w):
+    _, eng, ids = _engine(w)
+    d = eng._in("d", torch.tensor([[1, 2, 3]], dtype=torch.int32))
+    for _ in range(3):
+        eng.spec_verify(ids, d)
+    eng.sync()
+
+
+CASES = {"projections": projections, "draft": draft, "verify": verify}
+
+
+def main(argv):
+    if len(argv) != 1 or argv[0] not in CASES:
+        print(__doc__)
+        return 2
+    CASES[argv[0]](configs.WORKLOADS[WORKLOAD])
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main(sys.argv[1:]))
