@@ -35,7 +35,7 @@ sys.path.insert(0, ROOT)
 from speculative_decoding_spec_gb300 import configs, synth  # noqa: E402
 
 PERSISTENT = 0
-DRAFT_CLUSTER = 1
+DRAFT_CLUSTER = 0
 METRIC = "verify tok/s and HBM GB/s (% of roofline); effective tok/s at set acceptance"
 UNIT = "tok/s"
 
@@ -367,7 +367,7 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=20.0)
     ap.add_argument("--persistent", type=int, default=0,
                     help="1: one persistent kernel per target pass; 0: one kernel per step")
-    ap.add_argument("--draft-cluster", type=int, default=1,
+    ap.add_argument("--draft-cluster", type=int, default=0,
                     help="1: all drafter steps in one thread-block-cluster launch; 0: one kernel per operation")
     args = ap.parse_args()
     global PERSISTENT, DRAFT_CLUSTER

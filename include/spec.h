@@ -278,12 +278,12 @@ spec_status spec_set_graphs(spec_ctx *ctx, int32_t enable);
  *                       persistent pass, of the next step's weights or KV
  *                       pages before the grid barrier. */
 #define SPEC_OPT_PREFETCH 4
-/*  SPEC_OPT_DRAFT_CLUSTER (default 1) run all k drafter steps as one launch of
+/*  SPEC_OPT_DRAFT_CLUSTER (default 0) run all k drafter steps as one launch of
  *                       one thread-block cluster per sequence (weights
  *                       streamed through shared memory by bulk copies,
  *                       activations exchanged through distributed shared
  *                       memory); 0, or shapes it does not cover, run one
- *                       kernel per drafter operation. */
+ *                       kernel per drafter operation over the whole GPU. */
 #define SPEC_OPT_DRAFT_CLUSTER 5
 /*  SPEC_OPT_DRAFT_TRACE value = a device pointer to a uint64 buffer of at least
  *                       1 + k * (7 + 10 * n_drafter_layers) entries, or 0: the

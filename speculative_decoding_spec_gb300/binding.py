@@ -206,7 +206,7 @@ class Engine:
 
     def __init__(self, tw, dw=None, n_slots=1, B_max=1, rows_max=4, max_ctx=256, shuffle_pages=False,
                  device="cuda", graphs=True, persistent=False,
-                 draft_cluster=True):
+                 draft_cluster=False):
         L = lib()
         t = tw.shape
         self.tw, self.dw, self.shape = tw, dw, t

@@ -25,21 +25,23 @@ static int host_page_slots(int qn) {
   return ps > 0 ? ps : 1;
 }
 
-size_t attention_tc_smem(int hd, int qn) {
+// Query hi/lo tiles, the fp32 query rows and the r RoPE rows, then the page
+// slots or, after the rounds, the warp combine.
+size_t attention_tc_smem(int hd, int qn, int r) {
   const int qt = host_qt(qn), st = hd + 8, pw = host_page_slots(qn);
   const size_t pages = (size_t)2 * pw * PAGE * st * 2;
   const size_t combine = (size_t)ATT_WARPS * 16 * (hd + 2) * 4 + (size_t)qt * 16 * 4;
-  const size_t qstage = (size_t)(qn + 16) * hd * 4;  // fp32 query rows + RoPE rows
-  return (size_t)2 * qt * 16 * st * 2 + std::max(std::max(pages, combine), qstage);
+  const size_t qstage = (size_t)(qn + r) * hd * 4;
+  return (size_t)2 * qt * 16 * st * 2 + qstage + std::max(pages, combine);
 }
 
 // Shared memory of a CTA running the attention with `pw` page slots.
-size_t attention_tc_smem_slots(int hd, int qn, int pw) {
+size_t attention_tc_smem_slots(int hd, int qn, int r, int pw) {
   const int qt = host_qt(qn), st = hd + 8, kg = qt == 1 ? 4 : 1;
   const size_t pages = (size_t)2 * pw * PAGE * st * 2;
   const size_t combine = (size_t)qt * kg * pw * 16 * (hd + 2) * 4 + (size_t)qt * 16 * 4;
-  const size_t qstage = (size_t)(qn + 16) * hd * 4;
-  return (size_t)2 * qt * 16 * st * 2 + std::max(std::max(pages, combine), qstage);
+  const size_t qstage = (size_t)(qn + r) * hd * 4;
+  return (size_t)2 * qt * 16 * st * 2 + qstage + std::max(pages, combine);
 }
 
 void setup_attn_tc_attributes() {
@@ -65,7 +67,8 @@ int attention_tc(const AttnArgs& a, unsigned int* counters, int pps, cudaStream_
   const int qt = (QN + 15) / 16;
   // room for staging every split partial in the merge, when it fits
   const size_t merge = ((size_t)QN * a.n_split + 4) * 4 + (size_t)QN * a.n_split * a.hd * 4;
-  size_t smem = attention_tc_smem(a.hd, QN);
+  size_t smem = attention_tc_smem(a.hd, QN, a.R);
+  if (smem > 200 * 1024) return -2;
   if (merge <= 200 * 1024) smem = std::max(smem, merge);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.B * a.nkv, a.n_split);

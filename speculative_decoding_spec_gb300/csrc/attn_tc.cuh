@@ -10,8 +10,8 @@
 // Nano on Pixel with frozen multi-token prediction" (ai-news-spoon), section
 // "Zero-copy architecture").
 //
-// CTA (sequence b, KV head, split s) walks pages [s*pps, (s+1)*pps) with a
-// two-stage cp.async pipeline. All rows x GQA-group queries of the sequence
+// CTA (sequence b, KV head, split s) walks pages [s*pps, (s+1)*pps) in
+// rounds of cp.async loads (the first round in one burst with the queries). All rows x GQA-group queries of the sequence
 // form 16-query tiles, one warp per tile: S = Q K^T (scores), online softmax,
 // O += P V with V fragments from ldmatrix.trans. Q and P enter the MMAs as
 // bf16 hi + lo pairs (two MMAs each), so scores and outputs carry fp32-level
@@ -222,8 +222,10 @@ struct AttnTc {
     const bool active = warp < QT * KG * PW;
     __nv_bfloat16* Qh = reinterpret_cast<__nv_bfloat16*>(smem);
     __nv_bfloat16* Ql = Qh + QT * 16 * ST;
-    __nv_bfloat16* Kb = Ql + QT * 16 * ST;      // [PW][64][ST]
-    __nv_bfloat16* Vb = Kb + PW * PAGE * ST;    // [PW][64][ST]
+    float* qf = reinterpret_cast<float*>(Ql + QT * 16 * ST);  // [QN][HD] fp32 query rows
+    float* rf = qf + (size_t)QN * HD;                          // [R][HD] cos/sin rows
+    __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(rf + (size_t)a.R * HD);  // [PW][64][ST]
+    __nv_bfloat16* Vb = Kb + PW * PAGE * ST;                   // [PW][64][ST]
     __shared__ int s_last;
 
     const int slot = a.seq_ids[b];
@@ -232,12 +234,8 @@ struct AttnTc {
     const int npages = min((lmax + PAGE - 1) / PAGE, a.max_pages);
     const int p0 = split * pps, p1 = min(p0 + pps, npages);
     const __nv_bfloat16* base = (const __nv_bfloat16*)a.pool + (size_t)a.layer * a.layer_elems;
-    if (standalone) {
-      prefetch(a, pps, bx, by);
-      grid_dep_wait();
-      grid_dep_launch();
-    }
-    // the split's page ids, read once in parallel (and checked) when they fit
+    // the split's page ids (the block table does not change within a pass):
+    // read in parallel and checked before the dependency wait
     __shared__ int s_pgs[PGS_MAX];
     __shared__ int s_bad;
     const bool ids_cached = p1 - p0 <= PGS_MAX;
@@ -248,83 +246,23 @@ struct AttnTc {
       if (pg < 0 || pg >= a.n_pages) s_bad = 1;
       if (ids_cached) s_pgs[p - p0] = pg;
     }
+    if (standalone) {
+      prefetch(a, pps, bx, by);
+      grid_dep_wait();
+      grid_dep_launch();
+    }
     __syncthreads();
     const bool pages_ok = s_bad == 0;
     if (!pages_ok && threadIdx.x == 0) set_error(a.err, SPEC_ERR_CAPACITY);
     const int pend = pages_ok ? p1 : p0;
 
-    // queries: q = i*G + gg is head kvh*G + gg of row b*R + i. The fp32 rows
-    // (and RoPE rows when asked) are copied to shared memory in one burst
-    // (L2 only: they come from other CTAs of a persistent launch), then split
-    // into bf16 hi/lo with RoPE applied.
-    {
-      float* qf = reinterpret_cast<float*>(Kb);            // [QN][HD] (page buffers are free now)
-      float* rf = qf + (size_t)QN * HD;                    // [R][HD] cos/sin rows
-      for (int t = threadIdx.x; t < QN * (HD / 4); t += blockDim.x) {
-        const int q = t / (HD / 4), c4 = t % (HD / 4), i = q / G, gg = q % G;
-        cp_async16(qf + (size_t)q * HD + 4 * c4,
-                   a.q + (size_t)(b * a.R + i) * a.ldq + (kvh * G + gg) * HD + 4 * c4);
-      }
-      if (a.rope_cs)
-        for (int t = threadIdx.x; t < a.R * (HD / 4); t += blockDim.x) {
-          const int i = t / (HD / 4), c4 = t % (HD / 4);
-          cp_async16(rf + (size_t)i * HD + 4 * c4, a.rope_cs + (size_t)(b * a.R + i) * HD + 4 * c4);
-        }
-      cp_async_commit();
-      cp_async_wait<0>();
-      __syncthreads();
-      for (int t = threadIdx.x; t < QT * 16 * (HD / 2); t += blockDim.x) {
-        const int q = t / (HD / 2), d2 = (t % (HD / 2)) * 2;
-        float x0 = 0.f, x1 = 0.f;
-        if (q < QN) {
-          const float* qr = qf + (size_t)q * HD;
-          if (a.rope_cs) {
-            const float* cs = rf + (size_t)(q / G) * HD;
-            float v[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int d = d2 + e, half = HD / 2, j = d % half;
-              const float co = cs[2 * j], si = cs[2 * j + 1];
-              v[e] = d < half ? qr[d] * co - qr[d + half] * si : qr[d] * co + qr[d - half] * si;
-            }
-            x0 = v[0];
-            x1 = v[1];
-          } else {
-            x0 = qr[d2];
-            x1 = qr[d2 + 1];
-          }
-        }
-        uint32_t hi, lo;
-        split2(x0, x1, hi, lo);
-        *reinterpret_cast<uint32_t*>(Qh + q * ST + d2) = hi;
-        *reinterpret_cast<uint32_t*>(Ql + q * ST + d2) = lo;
-      }
-    }
-
-    const int r0 = 16 * qt + g, r1 = r0 + 8;
-    const int nk0 = r0 < QN ? L0 + r0 / G + a.key_extra : 0;
-    const int nk1 = r1 < QN ? L0 + r1 / G + a.key_extra : 0;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[NDT][4];
-#pragma unroll
-    for (int dt = 0; dt < NDT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
-    const float scale = rsqrtf((float)HD);
-
-    // rounds of up to PW pages: all loads of a round in flight, then compute
-    __shared__ int s_pg[16];
-    for (int rb = p0; rb < pend; rb += PW) {
-      const int nr = min(PW, pend - rb);
-      __syncthreads();
-      // page ids first: a copy must not wait for its own table lookup
-      if ((int)threadIdx.x < nr)
-        s_pg[threadIdx.x] =
-            ids_cached ? s_pgs[rb - p0 + threadIdx.x] : a.block_table[(size_t)slot * a.max_pages + rb + threadIdx.x];
-      __syncthreads();
-      constexpr int CPR = HD / 8;
+    // K and V of pages [rb, rb + nr) into the page slots (rows past the keys zeroed)
+    constexpr int CPR = HD / 8;
+    auto issue_pages = [&](int rb, int nr) {
       for (int t = threadIdx.x; t < nr * PAGE * CPR; t += blockDim.x) {
         const int ps = t / (PAGE * CPR), rr = (t / CPR) % PAGE, ch = t % CPR;
         const int p = rb + ps;
-        const int pg = s_pg[ps];
+        const int pg = ids_cached ? s_pgs[p - p0] : a.block_table[(size_t)slot * a.max_pages + p];
         const int nk = min(PAGE, lmax - p * PAGE);
         __nv_bfloat16* Ks = Kb + (size_t)ps * PAGE * ST;
         __nv_bfloat16* Vs = Vb + (size_t)ps * PAGE * ST;
@@ -338,9 +276,72 @@ struct AttnTc {
           *reinterpret_cast<uint4*>(Vs + rr * ST + ch * 8) = make_uint4(0, 0, 0, 0);
         }
       }
-      cp_async_commit();
-      cp_async_wait<0>();
+    };
+
+    // queries: q = i*G + gg is head kvh*G + gg of row b*R + i. The fp32 rows
+    // (and RoPE rows when asked) come to shared memory in one burst with the
+    // first round's pages (L2 only: they come from other CTAs or the previous
+    // kernel), then are split into bf16 hi/lo with RoPE applied.
+    for (int t = threadIdx.x; t < QN * (HD / 4); t += blockDim.x) {
+      const int q = t / (HD / 4), c4 = t % (HD / 4), i = q / G, gg = q % G;
+      cp_async16(qf + (size_t)q * HD + 4 * c4, a.q + (size_t)(b * a.R + i) * a.ldq + (kvh * G + gg) * HD + 4 * c4);
+    }
+    if (a.rope_cs)
+      for (int t = threadIdx.x; t < a.R * (HD / 4); t += blockDim.x) {
+        const int i = t / (HD / 4), c4 = t % (HD / 4);
+        cp_async16(rf + (size_t)i * HD + 4 * c4, a.rope_cs + (size_t)(b * a.R + i) * HD + 4 * c4);
+      }
+    if (p0 < pend) issue_pages(p0, min(PW, pend - p0));
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int t = threadIdx.x; t < QT * 16 * (HD / 2); t += blockDim.x) {
+      const int q = t / (HD / 2), d2 = (t % (HD / 2)) * 2;
+      float x0 = 0.f, x1 = 0.f;
+      if (q < QN) {
+        const float* qr = qf + (size_t)q * HD;
+        if (a.rope_cs) {
+          const float* cs = rf + (size_t)(q / G) * HD;
+          float v[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int d = d2 + e, half = HD / 2, j = d % half;
+            const float co = cs[2 * j], si = cs[2 * j + 1];
+            v[e] = d < half ? qr[d] * co - qr[d + half] * si : qr[d] * co + qr[d - half] * si;
+          }
+          x0 = v[0];
+          x1 = v[1];
+        } else {
+          x0 = qr[d2];
+          x1 = qr[d2 + 1];
+        }
+      }
+      uint32_t hi, lo;
+      split2(x0, x1, hi, lo);
+      *reinterpret_cast<uint32_t*>(Qh + q * ST + d2) = hi;
+      *reinterpret_cast<uint32_t*>(Ql + q * ST + d2) = lo;
+    }
+
+    const int r0 = 16 * qt + g, r1 = r0 + 8;
+    const int nk0 = r0 < QN ? L0 + r0 / G + a.key_extra : 0;
+    const int nk1 = r1 < QN ? L0 + r1 / G + a.key_extra : 0;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[NDT][4];
+#pragma unroll
+    for (int dt = 0; dt < NDT; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+    const float scale = rsqrtf((float)HD);
+
+    // rounds of up to PW pages: all loads of a round in flight, then compute
+    // (the first round's loads went with the queries)
+    for (int rb = p0; rb < pend; rb += PW) {
+      const int nr = min(PW, pend - rb);
       __syncthreads();
+      if (rb != p0) {
+        issue_pages(rb, nr);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+      }
       if (active && pslot < nr) {
         const __nv_bfloat16* Ks = Kb + (size_t)pslot * PAGE * ST;
         const __nv_bfloat16* Vs = Vb + (size_t)pslot * PAGE * ST;
@@ -414,16 +415,16 @@ struct AttnTc {
     }
     if (a.n_split == 1) return;
 
-    // the last split CTA of (b, KV head) merges
-    __threadfence();
+    // the last split CTA of (b, KV head) merges: the arrival is a release
+    // (this CTA's partials, ordered by the barrier) and an acquire (the other
+    // splits' partials) in one atomic
     __syncthreads();
     if (threadIdx.x == 0) {
-      const unsigned int done = atomicAdd(counters + bx, 1u);
+      const unsigned int done = atomic_add_acq_rel(counters + bx, 1u);
       s_last = done == (unsigned int)a.n_split - 1;
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     // split weights w[q][s] = e^(m_s - M_q) / L_q in shared memory; the split
     // partials of all queries are first copied to shared memory in one burst
     // (every request in flight) when they fit

@@ -1334,7 +1334,7 @@ bool draft_cluster_plan(DraftDesc& D) {
     if (D.kv_dtype == DT_BF16) {
       if (ncta % D.nkv) continue;
       for (int pw = 4; pw >= 1 && !pw_cap; --pw)
-        if (attention_tc_smem_slots(D.hd, G, pw) <= (size_t)ns * SLOT) pw_cap = pw;
+        if (attention_tc_smem_slots(D.hd, G, 1, pw) <= (size_t)ns * SLOT) pw_cap = pw;
       if (!pw_cap) continue;
     }
     size_t off = (size_t)ns * SLOT;

@@ -280,8 +280,8 @@ struct PassDesc {
 int pass_persistent(const PassDesc& d, cudaStream_t st);
 bool pass_persistent_supported(int hd, int max_rows);
 // tensor-core attention for bf16 caches (head_dim 64 or 128)
-size_t attention_tc_smem(int hd, int qn);
-size_t attention_tc_smem_slots(int hd, int qn, int pw);
+size_t attention_tc_smem(int hd, int qn, int r);
+size_t attention_tc_smem_slots(int hd, int qn, int r, int pw);
 void setup_attn_tc_attributes();
 int attention_tc_splits(int B, int nkv, int max_pages, int* pps, int qn);
 int attention_tc(const AttnArgs& a, unsigned int* counters, int pps, cudaStream_t st);

@@ -264,7 +264,7 @@ size_t pass_smem(const PassDesc& D) {
     s = std::max(s, tc::plan<MK_WARPS>(g, tc::MAP_PLAIN, D.nsm).smem);
   }
   const int qn = D.R * (D.nq / D.nkv);
-  s = std::max(s, attention_tc_smem(D.hd, qn));
+  s = std::max(s, attention_tc_smem(D.hd, qn, D.R));
   const size_t merge = ((size_t)qn * D.n_split + 4) * 4 + (size_t)qn * D.n_split * D.hd * 4;
   if (merge <= 200 * 1024) s = std::max(s, merge);
   return s;

@@ -160,7 +160,7 @@ struct spec_ctx {
   bool persistent = false;
   unsigned long long* trace = nullptr;
   bool prefetch = false;
-  bool draft_cluster = true;
+  bool draft_cluster = false;
   unsigned long long* dtrace = nullptr;
   int cluster_plan = 0;     // fused drafter layout: 0 not made yet, 1 made, -1 not supported
   DraftDesc cplan;
@@ -186,7 +186,10 @@ int run_attention(spec_ctx* c, AttnArgs at, cudaStream_t st) {
     int pps = 1;
     at.n_split = attention_tc_splits(at.B, at.nkv, c->kv.max_pages_per_seq, &pps, at.R * (at.nq / at.nkv));
     at.pages_per_split = pps;
-    return attention_tc(at, c->wk.attn_count, pps, st);
+    const int r = attention_tc(at, c->wk.attn_count, pps, st);
+    if (r != -2) return r;
+    at.n_split = c->kv.max_pages_per_seq;  // the CUDA-core kernel's split: one page each
+    at.pages_per_split = 1;
   }
   return attention(at, st);
 }

@@ -37,12 +37,12 @@ def models(request):
     return tw, dw, T, D, prompt, s0
 
 
-def _engine(tw, dw, graphs=True, persistent=False, draft_cluster=True):
+def _engine(tw, dw, graphs=True, persistent=False, draft_cluster=False):
     return binding.Engine(tw, dw, n_slots=2, B_max=2, rows_max=64, max_ctx=CAP, shuffle_pages=True,
                           graphs=graphs, persistent=persistent, draft_cluster=draft_cluster)
 
 
-def _prefilled(models, graphs=True, persistent=False, draft_cluster=True):
+def _prefilled(models, graphs=True, persistent=False, draft_cluster=False):
     tw, dw, T, D, prompt, s0 = models
     eng = _engine(tw, dw, graphs, persistent, draft_cluster)
     ids = eng.seq_ids([1])
@@ -161,7 +161,7 @@ def test_fused_drafter_is_one_launch(models):
     draft call (Q4_0 needs every reduction width to be a multiple of 256 and
     falls back to the per-operation kernels at width 64)."""
     tw, dw, T, D, prompt, s0 = models
-    eng, ids = _prefilled(models, graphs=False)
+    eng, ids = _prefilled(models, graphs=False, draft_cluster=True)
     before = eng.kernel_launches()
     eng.spec_draft(ids, 1, W.k)
     eng.sync()
