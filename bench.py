@@ -48,6 +48,27 @@ def peaks():
     return 6800.0, 1900.0, "fallback"
 
 
+def measured_traffic():
+    """DRAM bytes per launch of the roofline kernel from the committed ncu
+    summary, or None when the kernel's sources changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "gemv_tc_e2b_verify_projections_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if line.startswith("#") or not line.strip():
+            continue
+        k, v = line.split(None, 1)
+        kv[k] = v.strip()
+    h = hashlib.sha256()
+    for f in kv["sources"].split(","):
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    if h.hexdigest() != kv["sources_sha256"]:
+        return None
+    return float(kv["dram_bytes_read_plus_write_per_launch"])
+
+
 def verify_bytes(w: configs.Workload, ctx_lens):
     """Algorithmic bytes of one verify pass: every linear weight and the tied
     LM head once, plus KV read (keys/values of all committed positions, all
@@ -303,7 +324,8 @@ def run_gpu(args, w, rank, world):
         "roofline": {"kernel": "gemv_kernel (weight-streaming projection)", "bound": "hbm",
                      "achieved": gb_avg / (gms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                      "frac": gb_avg / (gms / 1e3) / 1e9 / hbm_peak, "peak_kind": peak_kind,
-                     "bytes_per_launch": gb_avg, "ms_per_launch": gms, "traffic": None},
+                     "bytes_per_launch": gb_avg, "ms_per_launch": gms,
+                     "traffic": measured_traffic() if w.name == configs.BENCH_WORKLOAD else None},
         "gpu_launches": launches,
         "persistent_pass": bool(PERSISTENT),
         "fused_drafter": bool(DRAFT_CLUSTER),

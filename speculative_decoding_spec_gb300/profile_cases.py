@@ -6,7 +6,10 @@
         run twice -- the launch sequence whose average the bench's roofline
         line reports. About 2.5 GB of weights, so nothing stays in L2.
     python -m speculative_decoding_spec_gb300.profile_cases draft
-        three calls of the fused drafter (k = 3) on the E2B-shaped workload.
+        three draft calls (k = 3) on the E2B-shaped workload, one kernel per
+        drafter operation (the default drafter).
+    python -m speculative_decoding_spec_gb300.profile_cases draft_cluster
+        the same with the one-cluster fused drafter.
     python -m speculative_decoding_spec_gb300.profile_cases verify
         three verify passes (k = 3) of the E2B-shaped workload.
 
@@ -49,11 +52,16 @@ def projections(w):
         torch.cuda.synchronize()
 
 
-def draft(w):
+def draft(w, cluster=False):
     _, eng, ids = _engine(w)
+    eng.set_option(binding.SPEC_OPT_DRAFT_CLUSTER, int(cluster))
     for _ in range(3):
         eng.spec_draft(ids, w.B, w.k)
     eng.sync()
+
+
+def draft_cluster(w):
+    draft(w, cluster=True)
 
 
 def verify(w):
@@ -64,7 +72,7 @@ def verify(w):
     eng.sync()
 
 
-CASES = {"projections": projections, "draft": draft, "verify": verify}
+CASES = {"projections": projections, "draft": draft, "draft_cluster": draft_cluster, "verify": verify}
 
 
 def main(argv):
