@@ -487,7 +487,7 @@ int gemv(const GemvArgs& a0, cudaStream_t st) {
       if (m0 + 8 < a0.M) a.tail.mode = TAIL_NONE;
     }
     int r = -2;
-    if (a.W.dtype == DT_BF16) r = gemv_tc(a, a.tc_fix, a.tc_cnt, st);
+    if (a.W.dtype == DT_BF16 || a.W.dtype == DT_Q4_0) r = gemv_tc(a, a.tc_fix, a.tc_cnt, st);
     if (r == -1 || (r == -2 && a.epi == EPI_ROPE)) return -1;
     if (r >= 0) {
       launched += r;

@@ -69,6 +69,50 @@ static SPEC_DEV uint32_t bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// fp16 inputs (the Q4_0 weights, dequantized in registers, and the matching
+// fp16 hi/lo activations), fp32 accumulate
+static SPEC_DEV void mma16816_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                  uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// A pair of activations as hi + lo halves of the MMA input type.
+template <bool Q4>
+static SPEC_DEV void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  if (Q4) {
+    const __half h0 = __float2half_rn(x0), h1 = __float2half_rn(x1);
+    const __half2 hh = __halves2half2(h0, h1);
+    const __half2 ll = __floats2half2_rn(x0 - __half2float(h0), x1 - __half2float(h1));
+    hi = *reinterpret_cast<const uint32_t*>(&hh);
+    lo = *reinterpret_cast<const uint32_t*>(&ll);
+  } else {
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+    hi = bf16x2(x0, x1);
+    lo = bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+  }
+}
+
+// Eight Q4_0 codes of one row (one nibble in each byte of `raw`: the low
+// nibble for elements 0..15 of the 32-value block, the high one for 16..31) as
+// four fp16 pairs of code - 8, exact: 0x6400 | code is the fp16 1024 + code,
+// and subtracting 1032 leaves the small integer. The block scale is applied to
+// the step's partial sum in fp32 (a step never crosses a block).
+static SPEC_DEV void codes8(uint2 raw, bool high, uint32_t (&v)[4]) {
+  const uint32_t n0 = (high ? raw.x >> 4 : raw.x) & 0x0F0F0F0Fu, n1 = (high ? raw.y >> 4 : raw.y) & 0x0F0F0F0Fu;
+  const uint32_t w[4] = {__byte_perm(n0, 0x6464u, 0x5140), __byte_perm(n0, 0x6464u, 0x5342),
+                         __byte_perm(n1, 0x6464u, 0x5140), __byte_perm(n1, 0x6464u, 0x5342)};
+  const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&w[i]), off);
+    v[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
 // first unit of CTA b
 // First unit of CTA b: every CTA owns whole 16-row tiles (the tile counts of
 // two CTAs differ by at most one), so no tile is split between CTAs and no
@@ -77,7 +121,11 @@ __device__ HOSTDEV_INLINE int unit_begin(int b, const SkPlan& p) {
   return (int)(((long long)b * p.T) / p.grid) * p.C;
 }
 
-template <int TW>
+// Q4: Q4_0 weights (codes and fp16 scales, K % 128 == 0): the codes enter
+// fp16 MMAs exactly as code - 8 and the activations as fp16 hi + lo; each
+// 32-column step is one block, whose scale multiplies the step's fp32 partial.
+// Otherwise bf16 weights and bf16 MMAs.
+template <int TW, bool Q4 = false>
 struct Sk {
   const GemvArgs& a;
   const SkPlan& p;
@@ -121,6 +169,28 @@ struct Sk {
     const int t = u / p.C, ch = u - t * p.C;
     const int k0 = ch * KCH, steps = min(4, (a.K - k0) / 32);
     const bool vg = ok_g(t, g), vg8 = ok_g8(t, g);
+    if (Q4) {
+      // step s is 32-value block 4*ch + s: this lane's 8 values are the
+      // nibbles of bytes 8*(q&1) .. +7 (low nibbles for q < 2, high for q >= 2);
+      // the unit's 4 block scales of a row are 8 contiguous bytes.
+      // wa[s] = {code bytes, code bytes, scale bits, unused}
+      const uint8_t* C = (const uint8_t*)a.W.data;
+      const uint16_t* S = (const uint16_t*)a.W.scales;
+      const size_t ra = (size_t)(vg ? row_g(t, g) : 0), rb = (size_t)(vg8 ? row_g8(t, g) : 0);
+      const uint8_t* ca = C + ra * (a.K / 2) + (size_t)ch * 64 + 8 * (q & 1);
+      const uint8_t* cb = C + rb * (a.K / 2) + (size_t)ch * 64 + 8 * (q & 1);
+      const uint2 sa = vg ? ldg_stream8(S + ra * (a.K / 32) + 4 * ch) : make_uint2(0, 0);
+      const uint2 sb = vg8 ? ldg_stream8(S + rb * (a.K / 32) + 4 * ch) : make_uint2(0, 0);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const uint2 xa = vg ? ldg_stream8(ca + s * 16) : make_uint2(0, 0);
+        const uint2 xb = vg8 ? ldg_stream8(cb + s * 16) : make_uint2(0, 0);
+        const uint32_t sba = (s < 2 ? sa.x : sa.y) >> (16 * (s & 1)), sbb = (s < 2 ? sb.x : sb.y) >> (16 * (s & 1));
+        wa[s] = make_uint4(xa.x, xa.y, sba & 0xFFFFu, 0u);
+        wb[s] = make_uint4(xb.x, xb.y, sbb & 0xFFFFu, 0u);
+      }
+      return;
+    }
     const __nv_bfloat16* W = (const __nv_bfloat16*)a.W.data;
     const __nv_bfloat16* rg = W + (size_t)(vg ? row_g(t, g) : 0) * a.K + k0 + 8 * q;
     const __nv_bfloat16* rg8 = W + (size_t)(vg8 ? row_g8(t, g) : 0) * a.K + k0 + 8 * q;
@@ -165,10 +235,29 @@ struct Sk {
         xh = *reinterpret_cast<const uint4*>(bh + s * 32);
         xl = *reinterpret_cast<const uint4*>(bl + s * 32);
       }
-      mma16816(c, wa[s].x, wb[s].x, wa[s].y, wb[s].y, xh.x, xh.y);
-      mma16816(c, wa[s].x, wb[s].x, wa[s].y, wb[s].y, xl.x, xl.y);
-      mma16816(c, wa[s].z, wb[s].z, wa[s].w, wb[s].w, xh.z, xh.w);
-      mma16816(c, wa[s].z, wb[s].z, wa[s].w, wb[s].w, xl.z, xl.w);
+      if (Q4) {
+        // exact codes through the MMAs, then each row's block scale in fp32
+        const bool high = q >= 2;
+        uint32_t va[4], vb[4];
+        codes8(make_uint2(wa[s].x, wa[s].y), high, va);
+        codes8(make_uint2(wb[s].x, wb[s].y), high, vb);
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816_f16(t, va[0], vb[0], va[1], vb[1], xh.x, xh.y);
+        mma16816_f16(t, va[0], vb[0], va[1], vb[1], xl.x, xl.y);
+        mma16816_f16(t, va[2], vb[2], va[3], vb[3], xh.z, xh.w);
+        mma16816_f16(t, va[2], vb[2], va[3], vb[3], xl.z, xl.w);
+        const float sa = __half2float(__ushort_as_half((unsigned short)wa[s].z));
+        const float sb = __half2float(__ushort_as_half((unsigned short)wb[s].z));
+        c[0] = fmaf(sa, t[0], c[0]);
+        c[1] = fmaf(sa, t[1], c[1]);
+        c[2] = fmaf(sb, t[2], c[2]);
+        c[3] = fmaf(sb, t[3], c[3]);
+      } else {
+        mma16816(c, wa[s].x, wb[s].x, wa[s].y, wb[s].y, xh.x, xh.y);
+        mma16816(c, wa[s].x, wb[s].x, wa[s].y, wb[s].y, xl.x, xl.y);
+        mma16816(c, wa[s].z, wb[s].z, wa[s].w, wb[s].w, xh.z, xh.w);
+        mma16816(c, wa[s].z, wb[s].z, wa[s].w, wb[s].w, xl.z, xl.w);
+      }
     }
   }
 
@@ -214,11 +303,7 @@ struct Sk {
         }
         uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
-          hi[i] = bf16x2(v[2 * i], v[2 * i + 1]);
-          lo[i] = bf16x2(v[2 * i] - __bfloat162float(h0), v[2 * i + 1] - __bfloat162float(h1));
-        }
+        for (int i = 0; i < 4; ++i) split_pair<Q4>(v[2 * i], v[2 * i + 1], hi[i], lo[i]);
         *reinterpret_cast<uint4*>(xhi + m * p.xs + c8) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(xlo + m * p.xs + c8) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
@@ -330,7 +415,7 @@ struct Sk {
     // towards L2 (capped) and put the first unit in flight before the wait
     uint4 wa[4], wb[4];
     if (standalone) {
-      if (a.prefetch) prefetch_slice(u0, u1);
+      if (a.prefetch && !Q4) prefetch_slice(u0, u1);
       if (wa_ < wb_) load_unit(wa_, wa, wb);
       grid_dep_wait();
       grid_dep_launch();
@@ -488,8 +573,8 @@ __host__ __device__ inline SkPlan plan(const GemvArgs& a, int map, int nsm) {
 }
 
 // Carve the dynamic shared memory for a projection CTA.
-template <int TW>
-__device__ inline void sk_bind(Sk<TW>& k, unsigned char* smem_raw, float* fix, unsigned int* cnt, int bid,
+template <int TW, bool Q4>
+__device__ inline void sk_bind(Sk<TW, Q4>& k, unsigned char* smem_raw, float* fix, unsigned int* cnt, int bid,
                                bool standalone) {
   const SkPlan& p = k.p;
   k.xhi = reinterpret_cast<uint16_t*>(smem_raw);

@@ -209,7 +209,7 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     n += r;                 \
   } while (0)
 
-  if (c->persistent && c->fused_rope && pass_persistent_supported(hd, M)) {
+  if (c->persistent && c->fused_rope && m.w_dtype == SPEC_BF16 && pass_persistent_supported(hd, M)) {
     PassDesc D = {};
     D.L = m.n_layers; D.d = d; D.nq = nq; D.nkv = nkv; D.hd = hd; D.ff = ff; D.V = m.vocab;
     D.eps = m.rms_eps; D.theta = m.rope_theta;
@@ -559,9 +559,10 @@ spec_status spec_init(const spec_model_desc* model, const spec_weights* weights,
   setup_attn_tc_attributes();
   setup_draft_attributes();
   // RoPE and the KV append run in the QKV projection's epilogue when that
-  // projection is the bf16 tensor-core kernel writing a bf16 cache
-  c->fused_rope = m.w_dtype == SPEC_BF16 && m.kv_dtype == SPEC_BF16 && m.head_dim % 16 == 0 &&
-                  m.d_model % 32 == 0;
+  // projection is the tensor-core kernel (bf16 or Q4_0) writing a bf16 cache
+  c->fused_rope = ((m.w_dtype == SPEC_BF16 && m.d_model % 32 == 0) ||
+                   (m.w_dtype == SPEC_Q4_0 && m.d_model % 128 == 0)) &&
+                  m.kv_dtype == SPEC_BF16 && m.head_dim % 16 == 0;
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(workspace, 0, need.bytes, st) != cudaSuccess) {
     delete c;
