@@ -341,33 +341,52 @@ struct Sk {
     if (map == MAP_ROPE) {
       const RopeEpi& e = a.rope;
       const int hpt = e.hd / 16, h = t / hpt, j = 8 * (t % hpt) + g, half = e.hd / 2;
+      const bool rot = h < e.nq + e.nkv, is_q = h < e.nq;
+      // every table read of both rows first (rotation, position, page), then
+      // the writes: the reads do not wait behind the writes
+      float co[2] = {1.f, 1.f}, si[2] = {0.f, 0.f};
+      int pos[2] = {0, 0}, page[2] = {-1, -1};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int m = 2 * q + i, am = a.m_base + m;
+        if (m >= a.M) continue;
+        if (rot) {
+          co[i] = __ldcg(e.rope_cs + (size_t)am * e.hd + 2 * j);
+          si[i] = __ldcg(e.rope_cs + (size_t)am * e.hd + 2 * j + 1);
+        }
+        if (!is_q) pos[i] = __ldcg(e.pos + am);
+      }
+      if (!is_q) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int m = 2 * q + i, am = a.m_base + m;
+          if (m >= a.M) continue;
+          const int slot = e.seq_ids[am / e.R], pidx = pos[i] / 64;
+          page[i] = pidx < e.max_pages ? e.block_table[(size_t)slot * e.max_pages + pidx] : -1;
+        }
+      }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int m = 2 * q + i;
         if (m >= a.M) continue;
-        const int am = a.m_base + m;
         float y0 = c[i], y1 = c[2 + i];
-        if (h < e.nq + e.nkv) {
-          const float co = __ldcg(e.rope_cs + (size_t)am * e.hd + 2 * j);
-          const float si = __ldcg(e.rope_cs + (size_t)am * e.hd + 2 * j + 1);
+        if (rot) {
           const float x0 = y0, x1 = y1;
-          y0 = x0 * co - x1 * si;
-          y1 = x1 * co + x0 * si;
+          y0 = x0 * co[i] - x1 * si[i];
+          y1 = x1 * co[i] + x0 * si[i];
         }
-        if (h < e.nq) {
+        if (is_q) {
           a.Y[(size_t)m * a.ldy + h * e.hd + j] = y0;
           a.Y[(size_t)m * a.ldy + h * e.hd + j + half] = y1;
         } else {
-          const int pos = __ldcg(e.pos + am), slot = e.seq_ids[am / e.R], pidx = pos / 64;
-          const int page = pidx < e.max_pages ? e.block_table[(size_t)slot * e.max_pages + pidx] : -1;
-          if (page < 0 || page >= e.n_pages) {
+          if (page[i] < 0 || page[i] >= e.n_pages) {
             set_error(e.err, SPEC_ERR_CAPACITY);
             continue;
           }
-          const int plane = h < e.nq + e.nkv ? 0 : 1;
+          const int plane = rot ? 0 : 1;
           const int kh = h - e.nq - plane * e.nkv;
           __nv_bfloat16* dst = (__nv_bfloat16*)e.pool + e.layer_off +
-                               ((((size_t)page * 2 + plane) * e.nkv + kh) * 64 + pos % 64) * e.hd;
+                               ((((size_t)page[i] * 2 + plane) * e.nkv + kh) * 64 + pos[i] % 64) * e.hd;
           dst[j] = __float2bfloat16_rn(y0);
           dst[j + half] = __float2bfloat16_rn(y1);
         }
@@ -384,6 +403,26 @@ struct Sk {
     }
     const int rows[2] = {row_g(t, g), row_g8(t, g)};
     const bool oks[2] = {ok_g(t, g), ok_g8(t, g)};
+    if (a.epi == EPI_ADD) {
+      // residual add: all four reads in flight before any write (the writes
+      // would otherwise order each read behind the previous write)
+      float old[4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int m = 2 * q + i;
+          old[2 * h + i] = oks[h] && m < a.M ? __ldcg(a.Y + (size_t)m * a.ldy + rows[h]) : 0.f;
+        }
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int m = 2 * q + i;
+          if (oks[h] && m < a.M) a.Y[(size_t)m * a.ldy + rows[h]] = old[2 * h + i] + c[2 * h + i];
+        }
+      return;
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       if (!oks[h]) continue;
@@ -394,7 +433,6 @@ struct Sk {
         const float v = c[2 * h + i];
         float* y = a.Y ? a.Y + (size_t)m * a.ldy + rows[h] : nullptr;
         if (a.epi == EPI_STORE) *y = v;
-        else if (a.epi == EPI_ADD) *y = __ldcg(y) + v;
         else {
           if (y) *y = v;
           const unsigned long long key = pack_best(v, (uint32_t)rows[h]);
