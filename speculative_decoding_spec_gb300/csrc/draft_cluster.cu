@@ -47,6 +47,7 @@
 
 #include "attn_tc.cuh"
 #include "common.cuh"
+#include "mbar.cuh"
 
 #define SPEC_HD __host__ __device__ __forceinline__
 
@@ -67,7 +68,7 @@ constexpr unsigned SPIN_LIMIT = 1u << 26;
 
 enum { PH_WIN, PH_WQ, PH_WO, PH_WGU, PH_WDOWN, PH_WOUT, PH_HEAD, PH_MEMB };
 
-// ---- cluster, mbarrier and bulk-copy primitives ---------------------------
+// ---- cluster primitives (mbarrier and bulk copies in mbar.cuh) -----------
 
 SPEC_DEV void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -84,7 +85,6 @@ SPEC_DEV unsigned cluster_ctas() {
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
-SPEC_DEV uint32_t sa(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 SPEC_DEV uint32_t remote(const void* p, unsigned rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(sa(p)), "r"(rank));
@@ -101,36 +101,6 @@ SPEC_DEV void st_remote4(const float* p, unsigned rank, float4 v) {
 SPEC_DEV void st_remote_u64(const unsigned long long* p, unsigned rank, unsigned long long v) {
   asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(remote(p, rank)), "l"(v) : "memory");
 }
-SPEC_DEV void mbar_init(uint64_t* b, unsigned count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(count) : "memory");
-}
-SPEC_DEV void mbar_init_fence() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
-SPEC_DEV void mbar_expect_tx(uint64_t* b, unsigned bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(bytes) : "memory");
-}
-SPEC_DEV bool mbar_test(uint64_t* b, unsigned parity) {
-  unsigned ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(sa(b)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Global -> this CTA's shared memory, completion counted on `bar` in bytes.
-SPEC_DEV void bulk_load(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   sa(dst)),
-               "l"(src), "r"(bytes), "r"(sa(bar))
-               : "memory");
-}
-
-SPEC_DEV unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // Bounded wait on an mbarrier phase; on a timeout the CTA aborts.
 SPEC_DEV bool wait_phase(uint64_t* b, unsigned parity, volatile int* abort_s, int* err) {
   for (unsigned it = 0; it < SPIN_LIMIT; ++it) {

@@ -1,0 +1,696 @@
+// gemm_wide.cu -- weight-streaming projection for 9..64 activation rows on the
+// fifth-generation tensor cores (tcgen05.mma, accumulators in tensor memory,
+// operands staged by TMA).
+//
+// Verification runs the k+1 positions of every sequence in one pass, so each
+// weight is read once for all B*(k+1) rows ("Gemma 4's MTP drafter explained"
+// (molayo1419.me), section "Why is generating one token at a time slow?"). With
+// batch 4-8 and k = 4 that is 20-40 rows: too many for register-fragment MMAs
+// to keep up with HBM, while a 128-row weight tile times a 16-64-row activation
+// tile is a natural tcgen05 shape (M = 128 weight rows, N = rows padded to 16).
+//
+// Data flow per CTA (one CTA of 6 warps per SM):
+//  - warp 0 (one thread): TMA producer. A ring of stages, each one 128 x 64
+//    bf16 weight tile and the matching 64 columns of the activation hi and lo
+//    planes, both in the 128-byte-swizzled K-major layout the MMA reads.
+//    Weights do not depend on earlier kernels, so the first stages' weight
+//    loads are issued before the programmatic-launch wait.
+//  - warp 1: owns the tensor memory (2 accumulators of 64 fp32 columns); one
+//    thread issues, per stage, 4 k-steps x (hi, lo) MMAs and commits the stage
+//    back to the producer and, at the end of a tile, the accumulator to the
+//    epilogue. The accumulators alternate so the epilogue of one tile
+//    overlaps the MMAs of the next.
+//  - warps 2-5: epilogue. tcgen05.ld gives thread r the tile's weight row r for
+//    every activation row; they apply the RMSNorm factor and the operation's
+//    epilogue (store, residual add, gated GELU, RoPE + KV append, argmax +
+//    accept), which are the ones of the register-fragment kernel.
+//
+// The activations enter as bf16 hi + lo planes (x = hi + lo to 2^-17), written
+// once per launch by a small preparation kernel that also applies the RMSNorm
+// gain and computes each row's 1/rms; so a result equals an fp32-activation dot
+// product of the bf16 weights, as in the register-fragment kernel.
+//
+// Work split: units are (tile, 64-column chunk) pairs in tile-major order and
+// CTA b owns the balanced range [U*b/G, U*(b+1)/G). A tile cut between CTAs is
+// summed by the last CTA to arrive (arrival counter per tile), in CTA order, so
+// results do not depend on timing.
+//
+// Every wait is bounded: on a timeout the CTA records SPEC_ERR_TIMEOUT, stops,
+// drains its own copies and MMAs, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "mbar.cuh"
+#include "tail.cuh"
+
+namespace spec {
+namespace wide {
+
+constexpr int TM = 128;              // weight rows per tile (MMA M)
+constexpr int KC = 64;               // K columns per stage (one 128-byte swizzle row of bf16)
+constexpr int NTHR = 192;            // 6 warps
+constexpr int EPI0 = 64;             // first epilogue thread
+constexpr int W_BYTES = TM * KC * 2; // 16 KB weight tile per stage
+constexpr int XCH_LD = TM + 1;       // exchange buffer row stride (floats): conflict-free both ways
+constexpr int MAX_STAGES = 8;
+constexpr int SMEM_LIMIT = 227 * 1024;
+constexpr unsigned SPIN_LIMIT = 1u << 26;
+constexpr int TMEM_COLS = 128;       // two accumulators of up to 64 columns
+
+enum { MAP_PLAIN = 0, MAP_PAIR = 1, MAP_ROPE = 2 };
+
+struct Plan {
+  int T, C, U, grid;
+  int MP;        // activation rows padded to a multiple of 16 (MMA N)
+  int map;
+  int stages;
+  int stage_bytes;
+  int smem;      // dynamic shared memory requested (includes 1 KB alignment slack)
+};
+
+// ---- tcgen05 / TMA primitives ----------------------------------------------
+
+SPEC_DEV void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+SPEC_DEV void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
+// layout (8-row groups of 1024 bytes, stride-dimension offset 1024 bytes);
+// bits 46-48 hold the fixed value 0b001, bits 61-63 the swizzle mode (2).
+SPEC_DEV uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at
+// bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+SPEC_DEV void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued so far is done.
+SPEC_DEV void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(sa(bar))
+               : "memory");
+}
+
+// 2-D tiled TMA load of box (x, y) -> shared memory, completion on `bar`.
+SPEC_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          sa(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(sa(bar))
+      : "memory");
+}
+
+// 16 consecutive accumulator columns of this warp's 32 lanes (lane = tile row).
+SPEC_DEV void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+SPEC_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Named barrier of the 4 epilogue warps.
+SPEC_DEV void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Bounded wait on an mbarrier phase; a timeout sets the abort flag and the
+// error word, and every other wait then gives up too.
+SPEC_DEV bool wait_phase(uint64_t* b, unsigned parity, volatile int* abort_s, int* err) {
+  for (unsigned it = 0; it < SPIN_LIMIT; ++it) {
+    if (mbar_test(b, parity)) return true;
+    if (*abort_s) return false;
+  }
+  *abort_s = 1;
+  set_error(err, SPEC_ERR_TIMEOUT);
+  return false;
+}
+// The same without giving up on abort: used to drain this CTA's own copies
+// and MMAs before it frees its shared and tensor memory.
+SPEC_DEV void drain_phase(uint64_t* b, unsigned parity) {
+  for (unsigned it = 0; it < SPIN_LIMIT; ++it)
+    if (mbar_test(b, parity)) return;
+}
+
+// ---- plan ----------------------------------------------------------------
+
+__host__ __device__ inline int unit_begin(int b, const Plan& p) { return (int)(((long long)b * p.U) / p.grid); }
+
+// CTA whose unit range holds unit u.
+__host__ __device__ inline int cta_of(int u, const Plan& p) {
+  int b = (int)((((long long)u + 1) * p.grid - 1) / p.U);
+  if (b >= p.grid) b = p.grid - 1;
+  while (b > 0 && unit_begin(b, p) > u) --b;
+  while (b + 1 < p.grid && unit_begin(b + 1, p) <= u) ++b;
+  return b;
+}
+
+// Segments of a unit range: maximal runs of units of one tile.
+struct SegIter {
+  int u, u1, C;
+  SPEC_DEV bool next(int& t, int& c0, int& c1) {
+    if (u >= u1) return false;
+    t = u / C;
+    const int e = min(u1, (t + 1) * C);
+    c0 = u - t * C;
+    c1 = e - t * C;
+    u = e;
+    return true;
+  }
+};
+
+// ---- one CTA ----------------------------------------------------------------
+
+template <int MP>
+struct Cta {
+  const GemvArgs& a;
+  const Plan& p;
+  const CUtensorMap* tmw;
+  const CUtensorMap* tmx;
+  const float* inv_rms;
+  float* fix;
+  unsigned int* cnt;
+  int* err;
+  unsigned char* stages;   // p.stages x p.stage_bytes, 1024-byte aligned
+  float* xch;              // [MP][XCH_LD]
+  uint64_t *full, *empty, *accf, *acce, *drain;
+  float* rms_s;            // [64]
+  uint32_t* tmem_slot;
+  volatile int* abort_s;
+  int* bc;                 // [4] broadcast words of the epilogue warps
+  uint32_t tmem;
+  int u0, u1;
+
+  SPEC_DEV unsigned char* stage(int s) const { return stages + (size_t)s * p.stage_bytes; }
+
+  SPEC_DEV void load_w(int s, int u) const {
+    const int t = u / p.C, x = (u - t * p.C) * KC;
+    unsigned char* dst = stage(s);
+    if (p.map == MAP_PAIR) {
+      // rows 0-63: gate rows 64t.., rows 64-127: the matching up rows
+      tma_load_2d(dst, tmw, x, t * 64, &full[s]);
+      tma_load_2d(dst + W_BYTES / 2, tmw, x, a.geglu_half + t * 64, &full[s]);
+    } else {
+      tma_load_2d(dst, tmw, x, t * TM, &full[s]);
+    }
+  }
+  SPEC_DEV void load_x(int s, int u) const {
+    const int t = u / p.C, x = (u - t * p.C) * KC;
+    tma_load_2d(stage(s) + W_BYTES, tmx, x, 0, &full[s]);
+  }
+
+  // warp 0, one thread
+  SPEC_DEV void producer() {
+    const int nu = u1 - u0, pre = min(nu, p.stages);
+    for (int n = 0; n < pre; ++n) {
+      mbar_expect_tx(&full[n], (unsigned)p.stage_bytes);
+      load_w(n, u0 + n);
+    }
+    grid_dep_wait();  // the activation planes come from the preparation kernel
+    for (int n = 0; n < pre; ++n) load_x(n, u0 + n);
+    int issued = pre;
+    for (int n = pre; n < nu; ++n) {
+      const int s = n % p.stages;
+      if (!wait_phase(&empty[s], ((n / p.stages) - 1) & 1, abort_s, err)) break;
+      mbar_expect_tx(&full[s], (unsigned)p.stage_bytes);
+      load_w(s, u0 + n);
+      load_x(s, u0 + n);
+      issued = n + 1;
+    }
+    if (*abort_s)  // let this CTA's copies land before its shared memory is released
+      for (int n = max(0, issued - p.stages); n < issued; ++n) drain_phase(&full[n % p.stages], (n / p.stages) & 1);
+  }
+
+  // warp 1, one thread
+  SPEC_DEV void mma_loop() {
+    const uint32_t idesc = idesc_bf16(TM, MP);
+    SegIter it{u0, u1, p.C};
+    int t, c0, c1, n = 0, i = 0;
+    bool ok = true;
+    while (ok && it.next(t, c0, c1)) {
+      const int acc = i & 1;
+      if (i >= 2 && !wait_phase(&acce[acc], ((i >> 1) - 1) & 1, abort_s, err)) break;
+      fence_after();
+      const uint32_t d = tmem + (uint32_t)(acc * 64);
+      for (int c = c0; c < c1; ++c, ++n) {
+        const int s = n % p.stages;
+        if (!wait_phase(&full[s], (n / p.stages) & 1, abort_s, err)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const uint32_t w = sa(stage(s)), xh = w + W_BYTES, xl = xh + MP * KC * 2;
+#pragma unroll
+        for (int ks = 0; ks < KC / 16; ++ks) {
+          const uint64_t ad = sw128_desc(w + 32 * ks);
+          mma_bf16(d, ad, sw128_desc(xh + 32 * ks), idesc, (c > c0 || ks > 0) ? 1u : 0u);
+          mma_bf16(d, ad, sw128_desc(xl + 32 * ks), idesc, 1u);
+        }
+        mma_commit(&empty[s]);
+      }
+      if (!ok) break;
+      mma_commit(&accf[acc]);
+      ++i;
+    }
+    // every MMA of this CTA complete before its tensor memory is freed
+    mma_commit(drain);
+    drain_phase(drain, 0);
+  }
+
+  // ---- epilogue (warps 2-5; thread r of the tile is TMEM lane r) ----
+
+  SPEC_DEV int row() const { return ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31); }
+
+  SPEC_DEV void store_add(int t, const float (&v)[MP]) {
+    const int n = t * TM + row();
+    if (n >= a.N) return;
+    if (a.epi == EPI_ADD) {
+      // residual add, 16 rows at a time: the reads in flight before the writes
+#pragma unroll
+      for (int g = 0; g < MP; g += 16) {
+        float old[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) old[i] = g + i < a.M ? __ldcg(a.Y + (size_t)(g + i) * a.ldy + n) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (g + i < a.M) a.Y[(size_t)(g + i) * a.ldy + n] = old[i] + v[g + i];
+      }
+      return;
+    }
+#pragma unroll
+    for (int m = 0; m < MP; ++m)
+      if (m < a.M) a.Y[(size_t)m * a.ldy + n] = v[m];
+  }
+
+  SPEC_DEV void argmax(int t, const float (&v)[MP], unsigned long long& mybest) {
+    const int r = row(), n = t * TM + r, e = threadIdx.x - EPI0;
+    if (a.Y && n < a.N) {
+#pragma unroll
+      for (int m = 0; m < MP; ++m)
+        if (m < a.M) a.Y[(size_t)m * a.ldy + n] = v[m];
+    }
+#pragma unroll
+    for (int m = 0; m < MP; ++m) xch[m * XCH_LD + r] = v[m];
+    epi_sync();
+    if (e < a.M) {
+      const int nv = min(TM, a.N - t * TM);
+      for (int j = 0; j < nv; ++j) {
+        const unsigned long long key = pack_best(xch[e * XCH_LD + j], (uint32_t)(t * TM + j));
+        mybest = key > mybest ? key : mybest;
+      }
+    }
+    epi_sync();
+  }
+
+  // gated GELU: tile rows 0-63 are gate rows j = 64t + r, rows 64-127 the up rows
+  SPEC_DEV void geglu(int t, const float (&v)[MP]) {
+    const int r = row();
+    if (r >= 64) {
+#pragma unroll
+      for (int m = 0; m < MP; ++m) xch[m * XCH_LD + (r - 64)] = v[m];
+    }
+    epi_sync();
+    const int j = t * 64 + r;
+    if (r < 64 && j < a.geglu_half) {
+#pragma unroll
+      for (int m = 0; m < MP; ++m)
+        if (m < a.M) {
+          const float g = v[m];
+          const float gl = 0.5f * g * (1.f + erff(g * 0.70710678118654752f));
+          a.Y[(size_t)m * a.ldy + j] = gl * xch[m * XCH_LD + r];
+        }
+    }
+    epi_sync();
+  }
+
+  // q, k, v head t (head_dim 128): rotate-half RoPE pairs element r with
+  // r +- 64; q goes to Y, k and v to the row's slot of the paged cache.
+  SPEC_DEV void rope(int t, float (&v)[MP]) {
+    const RopeEpi& E = a.rope;
+    const int r = row(), j = r & 63, h = t;
+    const bool second = r >= 64, rot = h < E.nq + E.nkv, is_q = h < E.nq;
+#pragma unroll
+    for (int m = 0; m < MP; ++m) xch[m * XCH_LD + r] = v[m];
+    epi_sync();
+    if (rot) {
+#pragma unroll
+      for (int m = 0; m < MP; ++m) {
+        if (m >= a.M) continue;
+        const int am = a.m_base + m;
+        const float co = __ldcg(E.rope_cs + (size_t)am * E.hd + 2 * j);
+        const float si = __ldcg(E.rope_cs + (size_t)am * E.hd + 2 * j + 1);
+        const float part = xch[m * XCH_LD + (r ^ 64)];
+        const float x0 = second ? part : v[m], x1 = second ? v[m] : part;
+        v[m] = second ? x1 * co + x0 * si : x0 * co - x1 * si;
+      }
+    }
+    epi_sync();
+    if (is_q) {
+#pragma unroll
+      for (int m = 0; m < MP; ++m)
+        if (m < a.M) a.Y[(size_t)m * a.ldy + h * E.hd + r] = v[m];
+      return;
+    }
+    const int plane = rot ? 0 : 1, kh = h - E.nq - plane * E.nkv;
+#pragma unroll
+    for (int m = 0; m < MP; ++m) {
+      if (m >= a.M) continue;
+      const int am = a.m_base + m;
+      const int pos = __ldcg(E.pos + am), slot = E.seq_ids[am / E.R], pidx = pos / 64;
+      const int page = pidx < E.max_pages ? E.block_table[(size_t)slot * E.max_pages + pidx] : -1;
+      if (page < 0 || page >= E.n_pages) {
+        set_error(E.err, SPEC_ERR_CAPACITY);
+        continue;
+      }
+      __nv_bfloat16* dst = (__nv_bfloat16*)E.pool + E.layer_off +
+                           ((((size_t)page * 2 + plane) * E.nkv + kh) * 64 + pos % 64) * E.hd;
+      dst[r] = __float2bfloat16_rn(v[m]);
+    }
+  }
+
+  SPEC_DEV void finish(int t, float (&v)[MP], unsigned long long& mybest) {
+#pragma unroll
+    for (int m = 0; m < MP; ++m) v[m] *= rms_s[m];
+    if (p.map == MAP_ROPE) rope(t, v);
+    else if (p.map == MAP_PAIR) geglu(t, v);
+    else if (a.epi == EPI_ARGMAX) argmax(t, v, mybest);
+    else store_add(t, v);
+  }
+
+  // A tile shared with other CTAs: publish this CTA's partial sum; the last
+  // CTA to arrive adds all of them in CTA order and finishes the tile.
+  SPEC_DEV void partial(int t, int i, float (&v)[MP], unsigned long long& mybest) {
+    const int r = row(), e = threadIdx.x - EPI0, b = blockIdx.x;
+    const int slot = t == u0 / p.C ? 0 : 1;
+    float* f = fix + (size_t)(b * 2 + slot) * MP * TM;
+#pragma unroll
+    for (int m = 0; m < MP; ++m)
+      if (m < a.M) __stcg(f + m * TM + r, v[m]);
+    epi_sync();
+    if (e == 0) bc[2 + (i & 1)] = (int)atomic_add_acq_rel(cnt + t, 1u);
+    epi_sync();
+    const int done = bc[2 + (i & 1)];
+    const int bf = cta_of(t * p.C, p), bl = cta_of(t * p.C + p.C - 1, p);
+    if (done != bl - bf) return;
+#pragma unroll
+    for (int m = 0; m < MP; ++m) v[m] = 0.f;
+    for (int bb = bf; bb <= bl; ++bb) {
+      const int s2 = t == unit_begin(bb, p) / p.C ? 0 : 1;
+      const float* g = fix + (size_t)(bb * 2 + s2) * MP * TM;
+#pragma unroll
+      for (int m = 0; m < MP; ++m)
+        if (m < a.M) v[m] += __ldcg(g + m * TM + r);
+    }
+    if (e == 0) cnt[t] = 0u;
+    finish(t, v, mybest);
+  }
+
+  SPEC_DEV void epilogue() {
+    const int e = threadIdx.x - EPI0;
+    grid_dep_wait();
+    grid_dep_launch();
+    if (e < 64) rms_s[e] = e < a.M ? __ldcg(inv_rms + e) : 0.f;
+    epi_sync();
+    unsigned long long mybest = 0ull;
+    SegIter it{u0, u1, p.C};
+    int t, c0, c1, i = 0;
+    while (it.next(t, c0, c1)) {
+      const int acc = i & 1;
+      if (e == 0) bc[i & 1] = wait_phase(&accf[acc], (i >> 1) & 1, abort_s, err) ? 1 : 0;
+      epi_sync();
+      if (!bc[i & 1]) break;
+      fence_after();
+      float v[MP];
+      const uint32_t taddr = tmem + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)(acc * 64);
+#pragma unroll
+      for (int j = 0; j < MP / 16; ++j) tmem_ld16(taddr + 16 * j, v + 16 * j);
+      tmem_wait_ld();
+      fence_before();
+      mbar_arrive(&acce[acc]);
+      if (c0 == 0 && c1 == p.C) finish(t, v, mybest);
+      else partial(t, i, v, mybest);
+      ++i;
+    }
+    if (a.epi == EPI_ARGMAX && e < a.M && mybest) atomicMax(a.best + e, mybest);
+  }
+};
+
+template <int MP>
+__global__ void __launch_bounds__(NTHR, 1)
+    wide_kernel(const __grid_constant__ GemvArgs a, const __grid_constant__ Plan p,
+                const __grid_constant__ CUtensorMap tmw,
+                const __grid_constant__ CUtensorMap tmx, const float* inv_rms, float* fix, unsigned int* cnt,
+                int* err) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t mis = sa(smem_raw) & 1023u;
+  unsigned char* base = smem_raw + (mis ? 1024 - mis : 0);
+  Cta<MP> k{a, p, &tmw, &tmx, inv_rms, fix, cnt, err};
+  k.stages = base;
+  k.xch = reinterpret_cast<float*>(base + (size_t)p.stages * p.stage_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(k.xch + MP * XCH_LD);
+  k.full = bars;
+  k.empty = bars + MAX_STAGES;
+  k.accf = bars + 2 * MAX_STAGES;
+  k.acce = k.accf + 2;
+  k.drain = k.acce + 2;
+  k.rms_s = reinterpret_cast<float*>(k.drain + 1);
+  k.tmem_slot = reinterpret_cast<uint32_t*>(k.rms_s + 64);
+  k.abort_s = reinterpret_cast<volatile int*>(k.tmem_slot + 1);
+  k.bc = const_cast<int*>(k.abort_s) + 1;
+  k.u0 = unit_begin(blockIdx.x, p);
+  k.u1 = unit_begin(blockIdx.x + 1, p);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&k.full[s], 1);
+      mbar_init(&k.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k.accf[i], 1);
+      mbar_init(&k.acce[i], 128);
+    }
+    mbar_init(k.drain, 1);
+    *k.abort_s = 0;
+    mbar_init_fence();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sa(k.tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  k.tmem = *k.tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) k.producer();
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) k.mma_loop();
+    __syncwarp();
+  } else {
+    k.epilogue();
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(k.tmem), "r"(TMEM_COLS) : "memory");
+  }
+  if (a.epi != EPI_ARGMAX || a.tail.mode == TAIL_NONE) return;
+  // the last CTA to finish runs the accept / commit / draft tail
+  grid_dep_wait();
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) k.bc[0] = atomicAdd(a.tail.counter, 1u) == (unsigned)p.grid - 1;
+  __syncthreads();
+  if (!k.bc[0]) return;
+  __threadfence();
+  run_tail(a.tail);
+}
+
+// Activation rows -> bf16 hi/lo planes [2][MP][K] (gain applied) and 1/rms
+// per row (1 without a gain, 0 for the padding rows, whose planes are zero).
+__global__ void __launch_bounds__(256) wide_prep_kernel(const float* X, int ldx, int M, int K, const float* gain,
+                                                        float eps, int MP, uint16_t* xs, float* rms) {
+  __shared__ float red[32];
+  const int m = blockIdx.x;
+  grid_dep_wait();
+  grid_dep_launch();
+  uint16_t* hi = xs + (size_t)m * K;
+  uint16_t* lo = xs + (size_t)(MP + m) * K;
+  if (m >= M) {
+    for (int c8 = threadIdx.x * 8; c8 < K; c8 += blockDim.x * 8) {
+      *reinterpret_cast<uint4*>(hi + c8) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(lo + c8) = make_uint4(0, 0, 0, 0);
+    }
+    if (threadIdx.x == 0) rms[m] = 0.f;
+    return;
+  }
+  float ss = 0.f;
+  for (int c8 = threadIdx.x * 8; c8 < K; c8 += blockDim.x * 8) {
+    const float4 u0 = __ldcg(reinterpret_cast<const float4*>(X + (size_t)m * ldx + c8));
+    const float4 u1 = __ldcg(reinterpret_cast<const float4*>(X + (size_t)m * ldx + c8 + 4));
+    float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    if (gain) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        ss = fmaf(v[i], v[i], ss);
+        v[i] *= gain[c8 + i];
+      }
+    }
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
+      const __nv_bfloat162 hh = __halves2bfloat162(h0, h1);
+      const __nv_bfloat162 ll =
+          __floats2bfloat162_rn(v[2 * i] - __bfloat162float(h0), v[2 * i + 1] - __bfloat162float(h1));
+      h[i] = *reinterpret_cast<const uint32_t*>(&hh);
+      l[i] = *reinterpret_cast<const uint32_t*>(&ll);
+    }
+    *reinterpret_cast<uint4*>(hi + c8) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo + c8) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+  if (gain) {
+    const float tot = block_sum(ss, red);
+    if (threadIdx.x == 0) rms[m] = rsqrtf(tot / (float)K + eps);
+  } else if (threadIdx.x == 0) {
+    rms[m] = 1.f;
+  }
+}
+
+// ---- host -------------------------------------------------------------------
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_once;
+
+void init_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+}
+
+// Row-major bf16 [rows][inner] as a 2-D tensor; boxes of box_rows x 64
+// columns land in the 128-byte swizzle layout. Rows past the end read as zero.
+bool encode(CUtensorMap* m, const void* base, int inner, int rows, int box_rows) {
+  if (!g_encode || ((uintptr_t)base & 15) || (inner * 2) % 16) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)KC, (cuuint32_t)box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t fixed_smem(int MP) { return (size_t)MP * XCH_LD * 4 + (2 * MAX_STAGES + 5) * 8 + 64 * 4 + 4 + 4 + 16 + 1024; }
+
+template <int MP>
+cudaError_t launch_mp(const cudaLaunchConfig_t& cfg, const GemvArgs& a, const Plan& p, const CUtensorMap& tmw,
+                      const CUtensorMap& tmx) {
+  return cudaLaunchKernelEx(&cfg, wide_kernel<MP>, a, p, tmw, tmx, (const float*)a.wide.rms, a.wide.fix, a.tc_cnt,
+                            a.wide.err);
+}
+
+}  // namespace
+
+bool make_plan(const GemvArgs& a, int nsm, Plan& p) {
+  p.map = a.epi == EPI_GEGLU ? MAP_PAIR : a.epi == EPI_ROPE ? MAP_ROPE : MAP_PLAIN;
+  if (a.K % KC || a.M < 1 || a.M > 64 || a.N < 1) return false;
+  if (p.map == MAP_ROPE && (a.rope.hd != TM || a.N != (a.rope.nq + 2 * a.rope.nkv) * a.rope.hd)) return false;
+  if (p.map == MAP_PAIR && (a.geglu_half < 1 || a.N != 2 * a.geglu_half)) return false;
+  p.T = p.map == MAP_PAIR ? (a.geglu_half + 63) / 64 : (a.N + TM - 1) / TM;
+  p.C = a.K / KC;
+  p.U = p.T * p.C;
+  p.grid = std::min(p.U, nsm);
+  p.MP = (a.M + 15) / 16 * 16;
+  p.stage_bytes = W_BYTES + 2 * p.MP * KC * 2;
+  const size_t fixed = fixed_smem(p.MP);
+  p.stages = (int)std::min<size_t>(MAX_STAGES, (SMEM_LIMIT - fixed) / p.stage_bytes);
+  if (p.stages < 2) return false;
+  p.smem = (int)(p.stages * (size_t)p.stage_bytes + fixed);
+  return true;
+}
+
+}  // namespace wide
+
+using namespace wide;
+
+void setup_gemv_wide_attributes() {
+  cudaFuncSetAttribute(wide_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+}
+
+size_t gemv_wide_fix_bytes() { return (size_t)num_sms() * 2 * 64 * TM * sizeof(float); }
+
+bool gemv_wide_ok(const GemvArgs& a) {
+  Plan p;
+  return a.W.dtype == DT_BF16 && a.wide.xs && a.wide.rms && a.wide.fix && a.tc_cnt && a.K <= a.wide.kmax &&
+         make_plan(a, num_sms(), p);
+}
+
+// M in 1..64 rows, bf16 weights, K % 64 == 0 (gemv_wide_ok). Launches the
+// activation preparation and the projection; returns 2, or -1 on an error.
+int gemv_wide(const GemvArgs& a, cudaStream_t st) {
+  std::call_once(g_once, init_encode);
+  Plan p;
+  if (!make_plan(a, num_sms(), p)) return -1;
+  CUtensorMap tmw, tmx;
+  if (!encode(&tmw, a.W.data, a.K, a.N, p.map == MAP_PAIR ? 64 : TM) ||
+      !encode(&tmx, a.wide.xs, a.K, 2 * p.MP, 2 * p.MP))
+    return -1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t pc = {};
+  pc.gridDim = dim3(p.MP);
+  pc.blockDim = dim3(256);
+  pc.stream = st;
+  pc.attrs = attr;
+  pc.numAttrs = a.pdl ? 1 : 0;
+  if (cudaLaunchKernelEx(&pc, wide_prep_kernel, a.X, a.ldx, a.M, a.K, a.gain, a.eps, p.MP, a.wide.xs, a.wide.rms) !=
+      cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = pc;
+  cfg.gridDim = dim3(p.grid);
+  cfg.blockDim = dim3(NTHR);
+  cfg.dynamicSmemBytes = p.smem;
+  cudaError_t e;
+  switch (p.MP) {
+    case 16: e = launch_mp<16>(cfg, a, p, tmw, tmx); break;
+    case 32: e = launch_mp<32>(cfg, a, p, tmw, tmx); break;
+    case 48: e = launch_mp<48>(cfg, a, p, tmw, tmx); break;
+    default: e = launch_mp<64>(cfg, a, p, tmw, tmx); break;
+  }
+  return e == cudaSuccess ? 2 : -1;
+}
+
+}  // namespace spec

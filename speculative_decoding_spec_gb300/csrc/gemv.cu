@@ -467,24 +467,37 @@ void set_attrs_wt() {
 
 void setup_gemv_attributes() {
   setup_gemv_tc_attributes();
+  setup_gemv_wide_attributes();
   set_attrs_wt<DT_F32>();
   set_attrs_wt<DT_BF16>();
   set_attrs_wt<DT_Q4_0>();
 }
 
-// M > 8 runs as several passes of at most 8 rows (each pass streams W again).
+// More than 8 rows of bf16 weights with the tcgen05 scratch present: passes of
+// up to 64 rows through the tcgen05 kernel (gemm_wide.cu), each streaming the
+// weights once. Otherwise passes of at most 8 rows (each streams W again).
 int gemv(const GemvArgs& a0, cudaStream_t st) {
   int launched = 0;
-  for (int m0 = 0; m0 < a0.M; m0 += 8) {
+  GemvArgs first = a0;
+  first.M = std::min(64, a0.M);
+  const bool wide = a0.M > 8 && gemv_wide_ok(first);
+  const int step = wide ? 64 : 8;
+  for (int m0 = 0; m0 < a0.M; m0 += step) {
     GemvArgs a = a0;
-    a.M = std::min(8, a0.M - m0);
+    a.M = std::min(step, a0.M - m0);
     a.X = a0.X + (size_t)m0 * a0.ldx;
     a.m_base = a0.m_base + m0;
     if (a.Y) a.Y = a0.Y + (size_t)m0 * a0.ldy;
     if (a0.epi == EPI_ARGMAX) {
       a.best = a0.best + m0;
       // only the last pass runs the tail, over every row
-      if (m0 + 8 < a0.M) a.tail.mode = TAIL_NONE;
+      if (m0 + step < a0.M) a.tail.mode = TAIL_NONE;
+    }
+    if (wide) {
+      const int r = gemv_wide(a, st);
+      if (r < 0) return -1;
+      launched += r;
+      continue;
     }
     int r = -2;
     if (a.W.dtype == DT_BF16 || a.W.dtype == DT_Q4_0) r = gemv_tc(a, a.tc_fix, a.tc_cnt, st);

@@ -69,6 +69,16 @@ struct TailArgs {
   int* err;
 };
 
+// Scratch of the tcgen05 projection for 9..64 rows (gemm_wide.cu); all null:
+// that path is not used and more rows run as passes of 8.
+struct WideScratch {
+  uint16_t* xs;             // [2][64][kmax] bf16 activation planes (hi, lo)
+  float* rms;               // [64] 1/rms per activation row
+  float* fix;               // gemv_wide_fix_bytes(): split-tile partial sums
+  int kmax;                 // largest K the planes hold
+  int* err;                 // device error word (timeouts), may be null
+};
+
 struct GemvArgs {
   const float* X;           // [M][ldx] fp32 activations
   int ldx, M, N, K;
@@ -87,6 +97,7 @@ struct GemvArgs {
   unsigned int* tc_cnt;     // tensor-core kernel: per-tile arrival counters, zero between launches
   int pdl;                  // launch with programmatic dependent launch
   int prefetch;             // tensor-core kernel: pull the CTA's weight slice to L2 first
+  WideScratch wide;         // tcgen05 path for more than 8 rows (bf16 weights)
 };
 int gemv(const GemvArgs& a, cudaStream_t st);
 
@@ -238,6 +249,12 @@ void setup_gemv_attributes();
 void setup_gemv_tc_attributes();
 int gemv_tc(const GemvArgs& a, float* fix, unsigned int* cnt, cudaStream_t st);
 size_t gemv_tc_fixup_bytes();
+void setup_gemv_wide_attributes();
+bool gemv_wide_ok(const GemvArgs& a);
+int gemv_wide(const GemvArgs& a, cudaStream_t st);
+size_t gemv_wide_fix_bytes();
+// bytes of WideScratch for activation planes of up to kmax columns (0 when kmax == 0)
+inline size_t gemv_wide_xs_bytes(int kmax) { return (size_t)2 * 64 * kmax * 2; }
 void setup_attn_attributes();
 void setup_draft_attributes();
 

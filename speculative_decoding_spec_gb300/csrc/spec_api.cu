@@ -39,6 +39,7 @@ struct Work {
   int* abort_flag;
   float* tc_fix;
   unsigned int* tc_cnt;
+  WideScratch wide;         // tcgen05 projection scratch (null when passes have <= 8 rows)
   int* err;
   // drafter
   float *d_cat, *d_u, *d_q, *d_att, *d_act, *d_h, *d_scores, *d_rope, *d_part_o, *d_part_ml;
@@ -87,6 +88,16 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
   w.tc_fix = b.take<float>(base, gemv_tc_fixup_bytes() / sizeof(float));
   w.tc_cnt = b.take<unsigned int>(base, tc_counters(m, d));
   w.err = b.take<int>(base, 4);
+  if (M > 8) {
+    // widest reduction of any projection: target d, q heads, FFN; drafter input [h; e], width, heads, FFN
+    int kmax = std::max({2 * m.d_model, m.n_q_heads * m.head_dim, m.d_ff});
+    if (d) kmax = std::max({kmax, d->hidden, d->n_q_heads * m.head_dim, d->d_ff});
+    w.wide.kmax = kmax;
+    w.wide.xs = b.take<uint16_t>(base, gemv_wide_xs_bytes(kmax) / 2);
+    w.wide.rms = b.take<float>(base, 64);
+    w.wide.fix = b.take<float>(base, gemv_wide_fix_bytes() / sizeof(float));
+    w.wide.err = w.err;
+  }
   if (d) {
     const int dq = d->n_q_heads * m.head_dim;
     w.d_cat = b.take<float>(base, (size_t)B_max * 2 * m.d_model);
@@ -442,6 +453,7 @@ int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* dr
 int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st) {
   g.tc_fix = c->wk.tc_fix;
   g.tc_cnt = c->wk.tc_cnt;
+  g.wide = c->wk.wide;
   g.prefetch = c->prefetch ? 1 : 0;
   return gemv(g, st);
 }
@@ -639,7 +651,9 @@ spec_status spec_inject_drafts(spec_ctx* c, int32_t B, const int32_t* seq_ids, i
 
 size_t spec_linear_workspace_bytes(int32_t N, int32_t K, int32_t M) {
   if (N <= 0 || K <= 0 || M <= 0) return 0;
-  return gemv_tc_fixup_bytes() + (((size_t)N / 8 + 64) * sizeof(unsigned int) + 255) / 256 * 256 + 256;
+  size_t n = gemv_tc_fixup_bytes() + (((size_t)N / 8 + 64) * sizeof(unsigned int) + 255) / 256 * 256 + 256;
+  if (M > 8) n += gemv_wide_fix_bytes() + gemv_wide_xs_bytes(K) + 64 * sizeof(float) + 3 * 256;
+  return n;
 }
 
 spec_status spec_linear(const spec_matrix* w, int32_t N, int32_t K, const float* x, int32_t M, const float* gain,
@@ -651,6 +665,16 @@ spec_status spec_linear(const spec_matrix* w, int32_t N, int32_t K, const float*
   g.epi = EPI_STORE; g.Y = y; g.ldy = N; g.pdl = 0; g.prefetch = 0;
   g.tc_fix = (float*)workspace;
   g.tc_cnt = (unsigned int*)((char*)workspace + gemv_tc_fixup_bytes());
+  if (M > 8) {
+    char* p = (char*)workspace + gemv_tc_fixup_bytes() +
+              (((size_t)N / 8 + 64) * sizeof(unsigned int) + 255) / 256 * 256 + 256;
+    g.wide.fix = (float*)p;
+    p += (gemv_wide_fix_bytes() + 255) / 256 * 256;
+    g.wide.xs = (uint16_t*)p;
+    p += (gemv_wide_xs_bytes(K) + 255) / 256 * 256;
+    g.wide.rms = (float*)p;
+    g.wide.kmax = K;
+  }
   static std::once_flag once;
   std::call_once(once, setup_gemv_attributes);
   if (gemv(g, (cudaStream_t)stream) < 0) return SPEC_ECUDA;

@@ -33,7 +33,7 @@ def _sub_rows(w, rows):
 
 
 @pytest.mark.parametrize("dtype", [configs.F32, configs.BF16, configs.Q4_0])
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 13, 40])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 13, 40, 64])
 @pytest.mark.parametrize("NK", [(300, 256), (1000, 1536), (97, 512), (2048, 64 * 32)])
 def test_linear_matches_oracle(dtype, M, NK):
     N, K = NK
@@ -74,6 +74,20 @@ def test_linear_rows_do_not_depend_on_M():
         part = binding.spec_linear(w, x[:M].contiguous())
         torch.cuda.synchronize()
         assert torch.equal(part, full[:M])
+
+
+def test_wide_rows_do_not_depend_on_M():
+    """Above 8 rows (bf16) the projection runs on tcgen05 with the rows padded
+    to a multiple of 16; a row's result is bitwise the same for every row
+    count of that path, so a batch's verify rows do not depend on the batch."""
+    g = torch.Generator(device="cuda").manual_seed(6)
+    w = synth.make_matrix(g, configs.BF16, 1, 1000, 1536, 0.02, "cuda")
+    x = _x(64, 1536, 10)
+    full = binding.spec_linear(w, x)
+    for M in (9, 16, 17, 33, 40, 48):
+        part = binding.spec_linear(w, x[:M].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(part, full[:M]), M
 
 
 @pytest.mark.parametrize("shape", ["e2b", "e4b", "dense30b"])
