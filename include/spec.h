@@ -291,6 +291,22 @@ spec_status spec_set_graphs(spec_ctx *ctx, int32_t enable);
  *                       stamps (ns) at its start, after each operation's last
  *                       weight chunk and after each cluster barrier. */
 #define SPEC_OPT_DRAFT_TRACE 6
+/*  SPEC_OPT_WIDE_TRACE  value = a device pointer to a zeroed uint64 buffer of at
+ *                       least 256 * n_SMs * 16 entries, or 0: the next 256
+ *                       enqueued launches of the tcgen05 projection (passes of
+ *                       more than 8 rows) record, per CTA, globaltimer stamps
+ *                       (ns) in 16 slots: 0 entry, 1 setup done, 2 producer past
+ *                       the launch dependency, 3 first stage consumed, 4 last
+ *                       MMA issued, 5 last accumulator ready, 6 epilogue done,
+ *                       7 tensor memory freed, 8 last split-tile partial
+ *                       written, 9 its arrival counted, 10 partials summed (the
+ *                       tile's last CTA), 11 that tile finished, 12 first
+ *                       accumulator ready, 13 first tile done; slots a CTA does
+ *                       not reach stay as they were. Launch i uses entries
+ *                       [i * n_SMs * 16, (i + 1) * n_SMs * 16). Stamps are taken
+ *                       when a launch runs; with graphs on, the launches of a
+ *                       captured shape keep the slots of their capture. */
+#define SPEC_OPT_WIDE_TRACE 7
 spec_status spec_set_option(spec_ctx *ctx, int32_t option, int64_t value);
 
 /* Number of kernels the library launched (or replayed inside graphs) since the

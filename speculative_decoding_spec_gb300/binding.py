@@ -25,6 +25,7 @@ EXPORTS = ["spec_workspace_bytes", "spec_init", "spec_prefill", "spec_draft", "s
            "spec_linear_workspace_bytes", "spec_linear_noalloc", "spec_set_option"]
 (SPEC_OPT_GRAPHS, SPEC_OPT_PERSISTENT, SPEC_OPT_TRACE, SPEC_OPT_PREFETCH, SPEC_OPT_DRAFT_CLUSTER,
  SPEC_OPT_DRAFT_TRACE) = 1, 2, 3, 4, 5, 6
+SPEC_OPT_WIDE_TRACE = 7
 SPEC_LINEAR_NOALLOC_MAX_ROWS = 523776
 
 

@@ -15,13 +15,18 @@
 //    planes, both in the 128-byte-swizzled K-major layout the MMA reads.
 //    Weights do not depend on earlier kernels, so the first stages' weight
 //    loads are issued before the programmatic-launch wait.
-//  - warp 1: owns the tensor memory (2 accumulators of 64 fp32 columns); one
-//    thread issues, per stage, 4 k-steps x (hi, lo) MMAs and commits the stage
-//    back to the producer and, at the end of a tile, the accumulator to the
-//    epilogue. The accumulators alternate so the epilogue of one tile
-//    overlaps the MMAs of the next.
+//  - warp 1: owns the tensor memory; one thread issues, per stage, one MMA per
+//    16-column k-step with N = 2 x rows (the hi and lo planes are consecutive
+//    rows of the B operand, so each k-step is one instruction) and commits the
+//    stage back to the producer and, at the end of a tile, the accumulator to
+//    the epilogue. Even and odd k-steps go to two independent accumulator
+//    chains: with a few dozen activation rows an MMA is short, and
+//    back-to-back MMAs into one accumulator would wait on each other. Two
+//    such accumulator sets alternate between tiles, so the epilogue of one
+//    tile overlaps the MMAs of the next.
 //  - warps 2-5: epilogue. tcgen05.ld gives thread r the tile's weight row r for
-//    every activation row; they apply the RMSNorm factor and the operation's
+//    every activation row (the sum of the two chains' hi and lo columns);
+//    they apply the RMSNorm factor and the operation's
 //    epilogue (store, residual add, gated GELU, RoPE + KV append, argmax +
 //    accept), which are the ones of the register-fragment kernel.
 //
@@ -58,9 +63,12 @@ constexpr int EPI0 = 64;             // first epilogue thread
 constexpr int W_BYTES = TM * KC * 2; // 16 KB weight tile per stage
 constexpr int XCH_LD = TM + 1;       // exchange buffer row stride (floats): conflict-free both ways
 constexpr int MAX_STAGES = 8;
+constexpr int NBARS = 2 * MAX_STAGES + 6;  // full, empty, 2 acc-full, 2 acc-empty, drain, pad to 16 bytes
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr unsigned SPIN_LIMIT = 1u << 26;
-constexpr int TMEM_COLS = 128;       // two accumulators of up to 64 columns
+constexpr int TMEM_COLS = 512;       // 2 accumulator sets x 2 chains x (hi, lo) x up to 64 columns
+constexpr int SET_COLS = 256;        // columns of one accumulator set
+constexpr int CHAIN_COLS = 128;      // columns of one chain (hi columns, then lo columns)
 
 enum { MAP_PLAIN = 0, MAP_PAIR = 1, MAP_ROPE = 2 };
 
@@ -129,6 +137,11 @@ SPEC_DEV void tmem_ld16(uint32_t taddr, float* v) {
 }
 SPEC_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Optional per-CTA timeline (globaltimer, ns): slot i of this CTA's 16.
+SPEC_DEV void stamp(unsigned long long* tr, int i) {
+  if (tr) tr[blockIdx.x * 16 + i] = globaltimer();
+}
+
 // Named barrier of the 4 epilogue warps.
 SPEC_DEV void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -189,10 +202,13 @@ struct Cta {
   float* fix;
   unsigned int* cnt;
   int* err;
+  unsigned long long* trace;
   unsigned char* stages;   // p.stages x p.stage_bytes, 1024-byte aligned
   float* xch;              // [MP][XCH_LD]
   uint64_t *full, *empty, *accf, *acce, *drain;
   float* rms_s;            // [64]
+  float* rope_s;           // MAP_ROPE: [M][128] the rows' RoPE (cos, sin) pairs
+  int *pos_s, *page_s;     // MAP_ROPE: [64] each row's position and cache page
   uint32_t* tmem_slot;
   volatile int* abort_s;
   int* bc;                 // [4] broadcast words of the epilogue warps
@@ -225,6 +241,7 @@ struct Cta {
       load_w(n, u0 + n);
     }
     grid_dep_wait();  // the activation planes come from the preparation kernel
+    stamp(trace, 2);
     for (int n = 0; n < pre; ++n) load_x(n, u0 + n);
     int issued = pre;
     for (int n = pre; n < nu; ++n) {
@@ -241,7 +258,7 @@ struct Cta {
 
   // warp 1, one thread
   SPEC_DEV void mma_loop() {
-    const uint32_t idesc = idesc_bf16(TM, MP);
+    const uint32_t idesc = idesc_bf16(TM, 2 * MP);
     SegIter it{u0, u1, p.C};
     int t, c0, c1, n = 0, i = 0;
     bool ok = true;
@@ -249,27 +266,27 @@ struct Cta {
       const int acc = i & 1;
       if (i >= 2 && !wait_phase(&acce[acc], ((i >> 1) - 1) & 1, abort_s, err)) break;
       fence_after();
-      const uint32_t d = tmem + (uint32_t)(acc * 64);
+      const uint32_t d = tmem + (uint32_t)(acc * SET_COLS);
       for (int c = c0; c < c1; ++c, ++n) {
         const int s = n % p.stages;
         if (!wait_phase(&full[s], (n / p.stages) & 1, abort_s, err)) {
           ok = false;
           break;
         }
+        if (n == 0) stamp(trace, 3);
         fence_after();
-        const uint32_t w = sa(stage(s)), xh = w + W_BYTES, xl = xh + MP * KC * 2;
+        const uint32_t w = sa(stage(s)), x = w + W_BYTES;
 #pragma unroll
-        for (int ks = 0; ks < KC / 16; ++ks) {
-          const uint64_t ad = sw128_desc(w + 32 * ks);
-          mma_bf16(d, ad, sw128_desc(xh + 32 * ks), idesc, (c > c0 || ks > 0) ? 1u : 0u);
-          mma_bf16(d, ad, sw128_desc(xl + 32 * ks), idesc, 1u);
-        }
+        for (int ks = 0; ks < KC / 16; ++ks)
+          mma_bf16(d + (uint32_t)((ks & 1) * CHAIN_COLS), sw128_desc(w + 32 * ks), sw128_desc(x + 32 * ks), idesc,
+                   (c > c0 || ks > 1) ? 1u : 0u);
         mma_commit(&empty[s]);
       }
       if (!ok) break;
       mma_commit(&accf[acc]);
       ++i;
     }
+    stamp(trace, 4);
     // every MMA of this CTA complete before its tensor memory is freed
     mma_commit(drain);
     drain_phase(drain, 0);
@@ -279,37 +296,48 @@ struct Cta {
 
   SPEC_DEV int row() const { return ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31); }
 
-  SPEC_DEV void store_add(int t, const float (&v)[MP]) {
-    const int n = t * TM + row();
+  // The finished tile goes through shared memory: xch[m][r] = row m of the
+  // activations, weight row r of the tile, RMSNorm factor applied. The
+  // operation's epilogue then runs as short loops over rows, so its code is
+  // compact (it runs once per tile, with a cold instruction cache) and every
+  // thread can take any (row, column) of the tile.
+  SPEC_DEV void finish(int t, const float (&v)[MP], unsigned long long& mybest) {
+    const int r = row(), e = threadIdx.x - EPI0;
+#pragma unroll
+    for (int m = 0; m < MP; ++m) xch[m * XCH_LD + r] = v[m] * rms_s[m];
+    epi_sync();
+    if (p.map == MAP_ROPE) rope(t, r);
+    else if (p.map == MAP_PAIR) geglu(t, e);
+    else if (a.epi == EPI_ARGMAX) argmax(t, r, e, mybest);
+    else store_add(t, r);
+    epi_sync();  // xch is free for the next tile
+  }
+
+  SPEC_DEV void store_add(int t, int r) {
+    const int n = t * TM + r;
     if (n >= a.N) return;
     if (a.epi == EPI_ADD) {
-      // residual add, 16 rows at a time: the reads in flight before the writes
+      // residual add, 32 rows at a time with the reads ahead of the writes
+      for (int m0 = 0; m0 < a.M; m0 += 32) {
+        float old[32];
 #pragma unroll
-      for (int g = 0; g < MP; g += 16) {
-        float old[16];
+        for (int i = 0; i < 32; ++i) old[i] = __ldcg(a.Y + (size_t)min(m0 + i, a.M - 1) * a.ldy + n);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) old[i] = g + i < a.M ? __ldcg(a.Y + (size_t)(g + i) * a.ldy + n) : 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (g + i < a.M) a.Y[(size_t)(g + i) * a.ldy + n] = old[i] + v[g + i];
+        for (int i = 0; i < 32; ++i)
+          if (m0 + i < a.M) a.Y[(size_t)(m0 + i) * a.ldy + n] = old[i] + xch[(m0 + i) * XCH_LD + r];
       }
       return;
     }
-#pragma unroll
-    for (int m = 0; m < MP; ++m)
-      if (m < a.M) a.Y[(size_t)m * a.ldy + n] = v[m];
+#pragma unroll 4
+    for (int m = 0; m < a.M; ++m) a.Y[(size_t)m * a.ldy + n] = xch[m * XCH_LD + r];
   }
 
-  SPEC_DEV void argmax(int t, const float (&v)[MP], unsigned long long& mybest) {
-    const int r = row(), n = t * TM + r, e = threadIdx.x - EPI0;
+  SPEC_DEV void argmax(int t, int r, int e, unsigned long long& mybest) {
+    const int n = t * TM + r;
     if (a.Y && n < a.N) {
-#pragma unroll
-      for (int m = 0; m < MP; ++m)
-        if (m < a.M) a.Y[(size_t)m * a.ldy + n] = v[m];
+#pragma unroll 4
+      for (int m = 0; m < a.M; ++m) a.Y[(size_t)m * a.ldy + n] = xch[m * XCH_LD + r];
     }
-#pragma unroll
-    for (int m = 0; m < MP; ++m) xch[m * XCH_LD + r] = v[m];
-    epi_sync();
     if (e < a.M) {
       const int nv = min(TM, a.N - t * TM);
       for (int j = 0; j < nv; ++j) {
@@ -317,82 +345,64 @@ struct Cta {
         mybest = key > mybest ? key : mybest;
       }
     }
-    epi_sync();
   }
 
-  // gated GELU: tile rows 0-63 are gate rows j = 64t + r, rows 64-127 the up rows
-  SPEC_DEV void geglu(int t, const float (&v)[MP]) {
-    const int r = row();
-    if (r >= 64) {
-#pragma unroll
-      for (int m = 0; m < MP; ++m) xch[m * XCH_LD + (r - 64)] = v[m];
+  // gated GELU: tile rows 0-63 are gate rows j = 64t + c, rows 64-127 the
+  // matching up rows; thread e takes column c = e % 64 of every other row
+  SPEC_DEV void geglu(int t, int e) {
+    const int c = e & 63, j = t * 64 + c;
+    if (j >= a.geglu_half) return;
+#pragma unroll 2
+    for (int m = e >> 6; m < a.M; m += 2) {
+      const float g = xch[m * XCH_LD + c];
+      const float gl = 0.5f * g * (1.f + erff(g * 0.70710678118654752f));
+      a.Y[(size_t)m * a.ldy + j] = gl * xch[m * XCH_LD + 64 + c];
     }
-    epi_sync();
-    const int j = t * 64 + r;
-    if (r < 64 && j < a.geglu_half) {
-#pragma unroll
-      for (int m = 0; m < MP; ++m)
-        if (m < a.M) {
-          const float g = v[m];
-          const float gl = 0.5f * g * (1.f + erff(g * 0.70710678118654752f));
-          a.Y[(size_t)m * a.ldy + j] = gl * xch[m * XCH_LD + r];
-        }
-    }
-    epi_sync();
   }
 
   // q, k, v head t (head_dim 128): rotate-half RoPE pairs element r with
   // r +- 64; q goes to Y, k and v to the row's slot of the paged cache.
-  SPEC_DEV void rope(int t, float (&v)[MP]) {
+  SPEC_DEV void rope(int t, int r) {
     const RopeEpi& E = a.rope;
-    const int r = row(), j = r & 63, h = t;
+    const int j = r & 63, h = t;
     const bool second = r >= 64, rot = h < E.nq + E.nkv, is_q = h < E.nq;
-#pragma unroll
-    for (int m = 0; m < MP; ++m) xch[m * XCH_LD + r] = v[m];
-    epi_sync();
-    if (rot) {
-#pragma unroll
-      for (int m = 0; m < MP; ++m) {
-        if (m >= a.M) continue;
-        const int am = a.m_base + m;
-        const float co = __ldcg(E.rope_cs + (size_t)am * E.hd + 2 * j);
-        const float si = __ldcg(E.rope_cs + (size_t)am * E.hd + 2 * j + 1);
-        const float part = xch[m * XCH_LD + (r ^ 64)];
-        const float x0 = second ? part : v[m], x1 = second ? v[m] : part;
-        v[m] = second ? x1 * co + x0 * si : x0 * co - x1 * si;
-      }
-    }
-    epi_sync();
-    if (is_q) {
-#pragma unroll
-      for (int m = 0; m < MP; ++m)
-        if (m < a.M) a.Y[(size_t)m * a.ldy + h * E.hd + r] = v[m];
-      return;
-    }
     const int plane = rot ? 0 : 1, kh = h - E.nq - plane * E.nkv;
-#pragma unroll
-    for (int m = 0; m < MP; ++m) {
-      if (m >= a.M) continue;
-      const int am = a.m_base + m;
-      const int pos = __ldcg(E.pos + am), slot = E.seq_ids[am / E.R], pidx = pos / 64;
-      const int page = pidx < E.max_pages ? E.block_table[(size_t)slot * E.max_pages + pidx] : -1;
+    // the rows' tables were loaded into shared memory at the epilogue start
+#pragma unroll 4
+    for (int m = 0; m < a.M; ++m) {
+      const float self = xch[m * XCH_LD + r], part = xch[m * XCH_LD + (r ^ 64)];
+      const float co = rope_s[m * TM + 2 * j], si = rope_s[m * TM + 2 * j + 1];
+      const float x0 = second ? part : self, x1 = second ? self : part;
+      const float y = rot ? (second ? x1 * co + x0 * si : x0 * co - x1 * si) : self;
+      if (is_q) {
+        a.Y[(size_t)m * a.ldy + h * E.hd + r] = y;
+        continue;
+      }
+      const int page = page_s[m], pos = pos_s[m];
       if (page < 0 || page >= E.n_pages) {
         set_error(E.err, SPEC_ERR_CAPACITY);
         continue;
       }
       __nv_bfloat16* dst = (__nv_bfloat16*)E.pool + E.layer_off +
                            ((((size_t)page * 2 + plane) * E.nkv + kh) * 64 + pos % 64) * E.hd;
-      dst[r] = __float2bfloat16_rn(v[m]);
+      dst[r] = __float2bfloat16_rn(y);
     }
   }
 
-  SPEC_DEV void finish(int t, float (&v)[MP], unsigned long long& mybest) {
-#pragma unroll
-    for (int m = 0; m < MP; ++m) v[m] *= rms_s[m];
-    if (p.map == MAP_ROPE) rope(t, v);
-    else if (p.map == MAP_PAIR) geglu(t, v);
-    else if (a.epi == EPI_ARGMAX) argmax(t, v, mybest);
-    else store_add(t, v);
+  // Per-launch tables of the RoPE epilogue, loaded while the weights stream.
+  SPEC_DEV void load_rope_tables() {
+    const RopeEpi& E = a.rope;
+    const int e = threadIdx.x - EPI0;
+    for (int idx = e; idx < a.M * (TM / 4); idx += 128) {
+      const int m = idx / (TM / 4), q = idx - m * (TM / 4);
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(E.rope_cs + (size_t)(a.m_base + m) * E.hd) + q);
+      *reinterpret_cast<float4*>(rope_s + m * TM + 4 * q) = v;
+    }
+    if (e < a.M) {
+      const int am = a.m_base + e, pos = __ldcg(E.pos + am), pidx = pos / 64;
+      pos_s[e] = pos;
+      page_s[e] = pidx < E.max_pages ? E.block_table[(size_t)E.seq_ids[am / E.R] * E.max_pages + pidx] : -1;
+    }
   }
 
   // A tile shared with other CTAs: publish this CTA's partial sum; the last
@@ -401,26 +411,41 @@ struct Cta {
     const int r = row(), e = threadIdx.x - EPI0, b = blockIdx.x;
     const int slot = t == u0 / p.C ? 0 : 1;
     float* f = fix + (size_t)(b * 2 + slot) * MP * TM;
+    // all MP rows (the padding rows' sums are exact zeros): no branch between
+    // the stores here or the loads below
 #pragma unroll
-    for (int m = 0; m < MP; ++m)
-      if (m < a.M) __stcg(f + m * TM + r, v[m]);
+    for (int m = 0; m < MP; ++m) __stcg(f + m * TM + r, v[m]);
     epi_sync();
+    if (e == 0) stamp(trace, 8);
     if (e == 0) bc[2 + (i & 1)] = (int)atomic_add_acq_rel(cnt + t, 1u);
     epi_sync();
+    if (e == 0) stamp(trace, 9);
     const int done = bc[2 + (i & 1)];
     const int bf = cta_of(t * p.C, p), bl = cta_of(t * p.C + p.C - 1, p);
     if (done != bl - bf) return;
 #pragma unroll
     for (int m = 0; m < MP; ++m) v[m] = 0.f;
-    for (int bb = bf; bb <= bl; ++bb) {
-      const int s2 = t == unit_begin(bb, p) / p.C ? 0 : 1;
-      const float* g = fix + (size_t)(bb * 2 + s2) * MP * TM;
+    // two contributors per round of loads, added in CTA order
+    for (int bb = bf; bb <= bl; bb += 2) {
+      const bool two = bb + 1 <= bl;
+      const float* g0 = fix + (size_t)(bb * 2 + (t == unit_begin(bb, p) / p.C ? 0 : 1)) * MP * TM;
+      const float* g1 = two ? fix + (size_t)((bb + 1) * 2 + (t == unit_begin(bb + 1, p) / p.C ? 0 : 1)) * MP * TM : g0;
+      float u0[MP], u1[MP];
 #pragma unroll
-      for (int m = 0; m < MP; ++m)
-        if (m < a.M) v[m] += __ldcg(g + m * TM + r);
+      for (int m = 0; m < MP; ++m) {
+        u0[m] = __ldcg(g0 + m * TM + r);
+        u1[m] = __ldcg(g1 + m * TM + r);
+      }
+#pragma unroll
+      for (int m = 0; m < MP; ++m) {
+        v[m] += u0[m];
+        if (two) v[m] += u1[m];
+      }
     }
     if (e == 0) cnt[t] = 0u;
+    if (e == 0) stamp(trace, 10);
     finish(t, v, mybest);
+    if (e == 0) stamp(trace, 11);
   }
 
   SPEC_DEV void epilogue() {
@@ -428,6 +453,7 @@ struct Cta {
     grid_dep_wait();
     grid_dep_launch();
     if (e < 64) rms_s[e] = e < a.M ? __ldcg(inv_rms + e) : 0.f;
+    if (p.map == MAP_ROPE) load_rope_tables();
     epi_sync();
     unsigned long long mybest = 0ull;
     SegIter it{u0, u1, p.C};
@@ -437,19 +463,31 @@ struct Cta {
       if (e == 0) bc[i & 1] = wait_phase(&accf[acc], (i >> 1) & 1, abort_s, err) ? 1 : 0;
       epi_sync();
       if (!bc[i & 1]) break;
+      if (e == 0) stamp(trace, i == 0 ? 12 : 5);
       fence_after();
       float v[MP];
-      const uint32_t taddr = tmem + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)(acc * 64);
+      const uint32_t taddr = tmem + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)(acc * SET_COLS);
 #pragma unroll
-      for (int j = 0; j < MP / 16; ++j) tmem_ld16(taddr + 16 * j, v + 16 * j);
-      tmem_wait_ld();
+      for (int j = 0; j < MP / 16; ++j) {
+        // (chain 0: hi + lo) + (chain 1: hi + lo)
+        float h0[16], l0[16], h1[16], l1[16];
+        tmem_ld16(taddr + 16 * j, h0);
+        tmem_ld16(taddr + MP + 16 * j, l0);
+        tmem_ld16(taddr + CHAIN_COLS + 16 * j, h1);
+        tmem_ld16(taddr + CHAIN_COLS + MP + 16 * j, l1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[16 * j + i] = (h0[i] + l0[i]) + (h1[i] + l1[i]);
+      }
       fence_before();
       mbar_arrive(&acce[acc]);
       if (c0 == 0 && c1 == p.C) finish(t, v, mybest);
       else partial(t, i, v, mybest);
+      if (i == 0 && e == 0) stamp(trace, 13);
       ++i;
     }
     if (a.epi == EPI_ARGMAX && e < a.M && mybest) atomicMax(a.best + e, mybest);
+    if (e == 0) stamp(trace, 6);
   }
 };
 
@@ -462,7 +500,8 @@ __global__ void __launch_bounds__(NTHR, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t mis = sa(smem_raw) & 1023u;
   unsigned char* base = smem_raw + (mis ? 1024 - mis : 0);
-  Cta<MP> k{a, p, &tmw, &tmx, inv_rms, fix, cnt, err};
+  Cta<MP> k{a, p, &tmw, &tmx, inv_rms, fix, cnt, err, a.wide.trace};
+  if (threadIdx.x == 0) stamp(k.trace, 0);
   k.stages = base;
   k.xch = reinterpret_cast<float*>(base + (size_t)p.stages * p.stage_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(k.xch + MP * XCH_LD);
@@ -471,8 +510,12 @@ __global__ void __launch_bounds__(NTHR, 1)
   k.accf = bars + 2 * MAX_STAGES;
   k.acce = k.accf + 2;
   k.drain = k.acce + 2;
-  k.rms_s = reinterpret_cast<float*>(k.drain + 1);
-  k.tmem_slot = reinterpret_cast<uint32_t*>(k.rms_s + 64);
+  k.rms_s = reinterpret_cast<float*>(bars + NBARS);
+  k.pos_s = reinterpret_cast<int*>(k.rms_s + 64);
+  k.page_s = k.pos_s + 64;
+  // 16-byte aligned: the exchange tile, barrier block and row tables are multiples of 16 bytes
+  k.rope_s = reinterpret_cast<float*>(k.page_s + 64);
+  k.tmem_slot = reinterpret_cast<uint32_t*>(k.rope_s + (p.map == MAP_ROPE ? MP * TM : 0));
   k.abort_s = reinterpret_cast<volatile int*>(k.tmem_slot + 1);
   k.bc = const_cast<int*>(k.abort_s) + 1;
   k.u0 = unit_begin(blockIdx.x, p);
@@ -502,6 +545,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   __syncthreads();
   fence_after();
   k.tmem = *k.tmem_slot;
+  if (threadIdx.x == 0) stamp(k.trace, 1);
 
   if (warp == 0) {
     if (lane == 0) k.producer();
@@ -517,6 +561,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   if (warp == 1) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(k.tmem), "r"(TMEM_COLS) : "memory");
+    if (lane == 0) stamp(k.trace, 7);
   }
   if (a.epi != EPI_ARGMAX || a.tail.mode == TAIL_NONE) return;
   // the last CTA to finish runs the accept / commit / draft tail
@@ -609,7 +654,11 @@ bool encode(CUtensorMap* m, const void* base, int inner, int rows, int box_rows)
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t fixed_smem(int MP) { return (size_t)MP * XCH_LD * 4 + (2 * MAX_STAGES + 5) * 8 + 64 * 4 + 4 + 4 + 16 + 1024; }
+// shared memory besides the stages: exchange tile, barriers, per-row tables,
+// the RoPE rows (RoPE epilogue only), tensor-memory slot, flags, 1 KB alignment
+size_t fixed_smem(int MP, bool rope) {
+  return (size_t)MP * XCH_LD * 4 + NBARS * 8 + 3 * 64 * 4 + (rope ? (size_t)MP * TM * 4 : 0) + 4 + 4 + 16 + 1024;
+}
 
 template <int MP>
 cudaError_t launch_mp(const cudaLaunchConfig_t& cfg, const GemvArgs& a, const Plan& p, const CUtensorMap& tmw,
@@ -631,7 +680,7 @@ bool make_plan(const GemvArgs& a, int nsm, Plan& p) {
   p.grid = std::min(p.U, nsm);
   p.MP = (a.M + 15) / 16 * 16;
   p.stage_bytes = W_BYTES + 2 * p.MP * KC * 2;
-  const size_t fixed = fixed_smem(p.MP);
+  const size_t fixed = fixed_smem(p.MP, p.map == MAP_ROPE);
   p.stages = (int)std::min<size_t>(MAX_STAGES, (SMEM_LIMIT - fixed) / p.stage_bytes);
   if (p.stages < 2) return false;
   p.smem = (int)(p.stages * (size_t)p.stage_bytes + fixed);

@@ -77,6 +77,7 @@ struct WideScratch {
   float* fix;               // gemv_wide_fix_bytes(): split-tile partial sums
   int kmax;                 // largest K the planes hold
   int* err;                 // device error word (timeouts), may be null
+  unsigned long long* trace;  // optional [grid][16] globaltimer stamps of this launch
 };
 
 struct GemvArgs {

@@ -53,6 +53,7 @@ struct Work {
 };
 
 constexpr int KMAX = 16;
+constexpr int WTRACE_LAUNCHES = 256;
 
 // Arrival counters of the tensor-core projection: one per 8 output rows of
 // the widest matrix the passes project with.
@@ -173,6 +174,8 @@ struct spec_ctx {
   bool prefetch = false;
   bool draft_cluster = false;
   unsigned long long* dtrace = nullptr;
+  unsigned long long* wtrace = nullptr;  // tcgen05 projection timelines (SPEC_OPT_WIDE_TRACE)
+  int wtrace_n = 0;
   int cluster_plan = 0;     // fused drafter layout: 0 not made yet, 1 made, -1 not supported
   DraftDesc cplan;
   long long launches = 0;
@@ -454,6 +457,8 @@ int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st) {
   g.tc_fix = c->wk.tc_fix;
   g.tc_cnt = c->wk.tc_cnt;
   g.wide = c->wk.wide;
+  if (c->wtrace && c->wtrace_n < WTRACE_LAUNCHES && g.M > 8)
+    g.wide.trace = c->wtrace + (size_t)(c->wtrace_n++) * num_sms() * 16;
   g.prefetch = c->prefetch ? 1 : 0;
   return gemv(g, st);
 }
@@ -731,6 +736,10 @@ spec_status spec_set_option(spec_ctx* c, int32_t option, int64_t value) {
   else if (option == SPEC_OPT_PREFETCH) c->prefetch = value != 0;
   else if (option == SPEC_OPT_DRAFT_CLUSTER) c->draft_cluster = value != 0;
   else if (option == SPEC_OPT_DRAFT_TRACE) c->dtrace = (unsigned long long*)(uintptr_t)value;
+  else if (option == SPEC_OPT_WIDE_TRACE) {
+    c->wtrace = (unsigned long long*)(uintptr_t)value;
+    c->wtrace_n = 0;
+  }
   else return SPEC_EINVAL;
   for (auto& kv : c->cache) cudaGraphExecDestroy(kv.second.exec);
   c->cache.clear();

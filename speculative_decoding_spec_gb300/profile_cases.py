@@ -5,6 +5,10 @@
         (24 layers x QKV, O, gate/up, down, then the LM head; M = 4 rows),
         run twice -- the launch sequence whose average the bench's roofline
         line reports. About 2.5 GB of weights, so nothing stays in L2.
+    python -m speculative_decoding_spec_gb300.profile_cases projections_wide
+        one layer of the E4B-shaped bf16 target (QKV, O, gate/up, down) and
+        its LM head at M = 40 rows (batch 8, k = 4): the tcgen05 path, run
+        twice. About 0.86 GB of weights, so nothing stays in L2.
     python -m speculative_decoding_spec_gb300.profile_cases draft
         three draft calls (k = 3) on the E2B-shaped workload, one kernel per
         drafter operation (the default drafter).
@@ -52,6 +56,20 @@ def projections(w):
         torch.cuda.synchronize()
 
 
+def projections_wide(w):
+    t = configs.E4B
+    g = torch.Generator(device="cuda").manual_seed(3)
+    M = 40
+    seq = [(synth.make_matrix(g, t.wdtype, 1, N, K, t.wstd, "cuda"), K)
+           for N, K in ((t.nqkv, t.d), (t.d, t.nq * t.hd), (2 * t.ff, t.d), (t.d, t.ff), (t.V, t.d))]
+    xs = {K: torch.randn((M, K), device="cuda") for _, K in seq}
+    ys = [torch.empty((M, W.N), device="cuda") for W, _ in seq]
+    for _ in range(2):
+        for (W, K), y in zip(seq, ys):
+            binding.spec_linear(W, xs[K], y=y)
+        torch.cuda.synchronize()
+
+
 def draft(w, cluster=False):
     _, eng, ids = _engine(w)
     eng.set_option(binding.SPEC_OPT_DRAFT_CLUSTER, int(cluster))
@@ -72,7 +90,7 @@ def verify(w):
     eng.sync()
 
 
-CASES = {"projections": projections, "draft": draft, "draft_cluster": draft_cluster, "verify": verify}
+CASES = {"projections": projections, "projections_wide": projections_wide, "draft": draft, "draft_cluster": draft_cluster, "verify": verify}
 
 
 def main(argv):
