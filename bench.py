@@ -163,6 +163,17 @@ def greedy_reference(eng, ids, w, n_tokens):
     return ref
 
 
+def roofline_kernel_name(w):
+    """The projection kernel the verify pass of this workload runs."""
+    t = w.target
+    if t.wdtype == configs.BF16 and w.M > 8:
+        return "wide_kernel (tcgen05 weight-streaming projection; each launch with its wide_prep_kernel)"
+    if t.wdtype in (configs.BF16, configs.Q4_0):
+        return "gemv_tc_kernel (mma.sync weight-streaming projection%s)" % (
+            ", in passes of 8 rows" if w.M > 8 else "")
+    return "gemv_kernel (CUDA-core weight-streaming projection)"
+
+
 def time_dominant_kernel(tw, w, device, reps=5):
     """Average duration of the weight-streaming projection as the verify runs
     it: every layer's QKV, O, gate/up and down projections and the LM head,
@@ -321,7 +332,7 @@ def run_gpu(args, w, rank, world):
         "e2e": {"value": rows * world / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": int(h_ids.numel() * 4 + h_draws.numel() * 4 + h_offs.numel() * 4),
                 "d2h_bytes_per_step": int(h_out.numel() * 4 + h_ne.numel() * 4)},
-        "roofline": {"kernel": "gemv_kernel (weight-streaming projection)", "bound": "hbm",
+        "roofline": {"kernel": roofline_kernel_name(w), "bound": "hbm",
                      "achieved": gb_avg / (gms / 1e3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
                      "frac": gb_avg / (gms / 1e3) / 1e9 / hbm_peak, "peak_kind": peak_kind,
                      "bytes_per_launch": gb_avg, "ms_per_launch": gms,

@@ -11,6 +11,14 @@ __global__ void __launch_bounds__(256) attn_tc_kernel(AttnArgs a, int pps, unsig
   AttnTc<HD>::run(a, pps, counters, smem, blockIdx.x, blockIdx.y, true, smem_bytes);
 }
 
+// Balanced launch: one CTA per SM over the flattened pages of every
+// (sequence, KV head) pair.
+template <int HD>
+__global__ void __launch_bounds__(256) attn_tc_bal_kernel(AttnArgs a, unsigned int* counters, size_t smem_bytes) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  AttnTc<HD>::run_balanced(a, counters, smem, smem_bytes);
+}
+
 }  // namespace atc
 
 using namespace atc;
@@ -47,6 +55,8 @@ size_t attention_tc_smem_slots(int hd, int qn, int r, int pw) {
 void setup_attn_tc_attributes() {
   cudaFuncSetAttribute(attn_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   cudaFuncSetAttribute(attn_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaFuncSetAttribute(attn_tc_bal_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaFuncSetAttribute(attn_tc_bal_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
 }
 
 // Splits of the page range: about one CTA per SM, at most 32 splits (the
@@ -62,16 +72,24 @@ int attention_tc_splits(int B, int nkv, int max_pages, int* pps, int qn) {
   return (max_pages + p - 1) / p;
 }
 
-int attention_tc(const AttnArgs& a, unsigned int* counters, int pps, cudaStream_t st) {
+int attention_tc(const AttnArgs& a0, unsigned int* counters, int pps, cudaStream_t st) {
+  AttnArgs a = a0;
   const int QN = a.R * (a.nq / a.nkv);
   const int qt = (QN + 15) / 16;
-  // room for staging every split partial in the merge, when it fits
-  const size_t merge = ((size_t)QN * a.n_split + 4) * 4 + (size_t)QN * a.n_split * a.hd * 4;
+  // balanced page ranges (one CTA per SM) up to 64 sequences; the partials
+  // then have one slot per page of a sequence (the callers' buffers hold
+  // max_pages splits per row and head)
+  const bool balanced = a.B <= 64;
+  if (balanced) a.n_split = a.max_pages;
   size_t smem = attention_tc_smem(a.hd, QN, a.R);
   if (smem > 200 * 1024) return -2;
-  if (merge <= 200 * 1024) smem = std::max(smem, merge);
+  if (!balanced) {
+    // room for staging every split partial in the merge, when it fits
+    const size_t merge = ((size_t)QN * a.n_split + 4) * 4 + (size_t)QN * a.n_split * a.hd * 4;
+    if (merge <= 200 * 1024) smem = std::max(smem, merge);
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.B * a.nkv, a.n_split);
+  cfg.gridDim = balanced ? dim3(num_sms()) : dim3(a.B * a.nkv, a.n_split);
   cfg.blockDim = dim3(ATT_WARPS * 32);
   (void)qt;
   cfg.dynamicSmemBytes = smem;
@@ -82,8 +100,12 @@ int attention_tc(const AttnArgs& a, unsigned int* counters, int pps, cudaStream_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (a.hd == 128) e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<128>, a, pps, counters, smem);
-  else if (a.hd == 64) e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<64>, a, pps, counters, smem);
+  if (a.hd == 128)
+    e = balanced ? cudaLaunchKernelEx(&cfg, attn_tc_bal_kernel<128>, a, counters, smem)
+                 : cudaLaunchKernelEx(&cfg, attn_tc_kernel<128>, a, pps, counters, smem);
+  else if (a.hd == 64)
+    e = balanced ? cudaLaunchKernelEx(&cfg, attn_tc_bal_kernel<64>, a, counters, smem)
+                 : cudaLaunchKernelEx(&cfg, attn_tc_kernel<64>, a, pps, counters, smem);
   else return -2;
   return e == cudaSuccess ? 1 : -1;
 }

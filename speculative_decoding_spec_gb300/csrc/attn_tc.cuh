@@ -10,7 +10,7 @@
 // Nano on Pixel with frozen multi-token prediction" (ai-news-spoon), section
 // "Zero-copy architecture").
 //
-// CTA (sequence b, KV head, split s) walks pages [s*pps, (s+1)*pps) in
+// A split (sequence b, KV head, page range) walks its pages in
 // rounds of cp.async loads (the first round in one burst with the queries). All rows x GQA-group queries of the sequence
 // form 16-query tiles, one warp per tile: S = Q K^T (scores), online softmax,
 // O += P V with V fragments from ldmatrix.trans. Q and P enter the MMAs as
@@ -212,7 +212,82 @@ struct AttnTc {
   // CTA's warps could fill.
   static SPEC_DEV void run(const AttnArgs& a, int pps, unsigned int* counters, unsigned char* smem, int bx,
                            int by, bool standalone, size_t smem_bytes, int pw_cap = 0) {
-    const int b = bx / a.nkv, kvh = bx % a.nkv, split = by;
+    const int b = bx / a.nkv;
+    const int slot = a.seq_ids[b];
+    const int lmax = a.seq_len[slot] + a.R - 1 + a.key_extra;
+    const int npages = min((lmax + PAGE - 1) / PAGE, a.max_pages);
+    const int p0 = by * pps, p1 = min(p0 + pps, npages);
+    if (standalone) prefetch(a, pps, bx, by);
+    run_split(a, bx, p0, p1, by, a.n_split, counters, smem, standalone, smem_bytes, pw_cap);
+  }
+
+  // Balanced stand-alone launch: the pages of all (sequence, KV head) pairs,
+  // pair-major, are cut into equal contiguous ranges, one per CTA (at least a
+  // round of page slots each, so with few pages fewer CTAs work). A CTA's
+  // piece of a pair is one split of that pair; a pair's splits are numbered
+  // by CTA, so their partials and the merge order do not depend on timing.
+  static SPEC_DEV void run_balanced(const AttnArgs& a, unsigned int* counters, unsigned char* smem,
+                                    size_t smem_bytes) {
+    __shared__ int s_np[64];        // pages of each sequence
+    __shared__ long long s_off[65]; // first flattened page of each sequence
+    const int nkv = a.nkv, B = a.B;
+    const int G = a.nq / nkv, QT = (a.R * G + 15) / 16;
+    const int PW = page_slots(QT, blockDim.x >> 5);
+    if ((int)threadIdx.x < B) {
+      const int lmax = a.seq_len[a.seq_ids[threadIdx.x]] + a.R - 1 + a.key_extra;
+      s_np[threadIdx.x] = min((lmax + PAGE - 1) / PAGE, a.max_pages);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      long long acc = 0;
+      for (int b = 0; b < B; ++b) {
+        s_off[b] = acc;
+        acc += (long long)s_np[b] * nkv;
+      }
+      s_off[B] = acc;
+    }
+    __syncthreads();
+    const long long P = s_off[B];
+    const long long want = (P + PW - 1) / PW;
+    const int ncta = (int)(want < (long long)gridDim.x ? want : (long long)gridDim.x);
+    const int cta = blockIdx.x;
+    if (cta >= ncta) {
+      grid_dep_wait();
+      grid_dep_launch();
+      return;
+    }
+    auto begin = [&](int k) { return (P * k) / ncta; };
+    // CTA whose range holds flattened page q
+    auto owner = [&](long long q) {
+      int k = (int)(((q + 1) * ncta - 1) / P);
+      if (k >= ncta) k = ncta - 1;
+      while (k > 0 && begin(k) > q) --k;
+      while (k + 1 < ncta && begin(k + 1) <= q) ++k;
+      return k;
+    };
+    const long long q0 = begin(cta), q1 = begin(cta + 1);
+    int b = 0;
+    for (long long q = q0; q < q1;) {
+      // sequence of flattened page q: the first b with s_off[b + 1] > q
+      while (b + 1 < B && s_off[b + 1] <= q) ++b;
+      const int np = s_np[b];
+      const int kvh = (int)((q - s_off[b]) / np);
+      const long long pair_first = s_off[b] + (long long)kvh * np;
+      const long long pair_end = pair_first + np;
+      const long long e = q1 < pair_end ? q1 : pair_end;
+      const int k0 = owner(pair_first), k1 = owner(pair_end - 1);
+      run_split(a, b * nkv + kvh, (int)(q - pair_first), (int)(e - pair_first), cta - k0, k1 - k0 + 1, counters,
+                smem, true, smem_bytes, 0);
+      q = e;
+    }
+  }
+
+  // One split of (sequence, KV head) bx: pages [p0, p1) as split `split` of
+  // `nsplit`; partials are indexed with stride a.n_split (>= nsplit).
+  static SPEC_DEV void run_split(const AttnArgs& a, int bx, int p0, int p1, int split, int nsplit,
+                                 unsigned int* counters, unsigned char* smem, bool standalone, size_t smem_bytes,
+                                 int pw_cap) {
+    const int b = bx / a.nkv, kvh = bx % a.nkv;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, c = lane & 3;
     const int NW = blockDim.x >> 5;
     const int G = a.nq / a.nkv, QN = a.R * G, QT = (QN + 15) / 16;
@@ -231,8 +306,6 @@ struct AttnTc {
     const int slot = a.seq_ids[b];
     const int L0 = a.seq_len[slot];
     const int lmax = L0 + a.R - 1 + a.key_extra;  // keys of the last row
-    const int npages = min((lmax + PAGE - 1) / PAGE, a.max_pages);
-    const int p0 = split * pps, p1 = min(p0 + pps, npages);
     const __nv_bfloat16* base = (const __nv_bfloat16*)a.pool + (size_t)a.layer * a.layer_elems;
     // the split's page ids (the block table does not change within a pass):
     // read in parallel and checked before the dependency wait
@@ -247,7 +320,6 @@ struct AttnTc {
       if (ids_cached) s_pgs[p - p0] = pg;
     }
     if (standalone) {
-      prefetch(a, pps, bx, by);
       grid_dep_wait();
       grid_dep_launch();
     }
@@ -402,7 +474,7 @@ struct AttnTc {
       const float L = scr[((size_t)qq * 16 + row) * RS + HD + 1];
       const int i = q / G, gg = q % G;
       const int m = b * a.R + i, h = kvh * G + gg;
-      if (a.n_split == 1) {
+      if (nsplit == 1) {
         a.out[(size_t)m * a.nq * HD + h * HD + d] = L > 0.f ? acc / L : 0.f;
       } else {
         const size_t pidx = ((size_t)m * a.nq + h) * a.n_split + split;
@@ -413,7 +485,7 @@ struct AttnTc {
         }
       }
     }
-    if (a.n_split == 1) return;
+    if (nsplit == 1) return;
 
     // the last split CTA of (b, KV head) merges: the arrival is a release
     // (this CTA's partials, ordered by the barrier) and an acquire (the other
@@ -421,7 +493,7 @@ struct AttnTc {
     __syncthreads();
     if (threadIdx.x == 0) {
       const unsigned int done = atomic_add_acq_rel(counters + bx, 1u);
-      s_last = done == (unsigned int)a.n_split - 1;
+      s_last = done == (unsigned int)nsplit - 1;
     }
     __syncthreads();
     if (!s_last) return;
@@ -429,22 +501,22 @@ struct AttnTc {
     // partials of all queries are first copied to shared memory in one burst
     // (every request in flight) when they fit
     float* wts = reinterpret_cast<float*>(smem);                  // [QN][n_split]
-    float* pst = wts + ((QN * a.n_split + 3) & ~3);               // [QN][n_split][HD]
-    const size_t pbytes = (size_t)QN * a.n_split * HD * 4;
+    float* pst = wts + ((QN * nsplit + 3) & ~3);               // [QN][n_split][HD]
+    const size_t pbytes = (size_t)QN * nsplit * HD * 4;
     const bool staged = (size_t)((unsigned char*)pst - smem) + pbytes <= smem_bytes;
     if (staged) {
-      for (int t = threadIdx.x; t < QN * a.n_split * (HD / 4); t += blockDim.x) {
-        const int q = t / (a.n_split * (HD / 4)), r = t % (a.n_split * (HD / 4));
+      for (int t = threadIdx.x; t < QN * nsplit * (HD / 4); t += blockDim.x) {
+        const int q = t / (nsplit * (HD / 4)), r = t % (nsplit * (HD / 4));
         const int sp = r / (HD / 4), c4 = r % (HD / 4), i = q / G, gg = q % G;
         const size_t pi = ((size_t)(b * a.R + i) * a.nq + kvh * G + gg) * a.n_split + sp;
-        cp_async16(pst + ((size_t)q * a.n_split + sp) * HD + 4 * c4, a.part_o + pi * HD + 4 * c4);
+        cp_async16(pst + ((size_t)q * nsplit + sp) * HD + 4 * c4, a.part_o + pi * HD + 4 * c4);
       }
       cp_async_commit();
     }
-    float* lsp = pst + (staged ? (size_t)QN * a.n_split * HD : 0);   // [QN][n_split] split sums
-    const bool lsm = (size_t)((unsigned char*)(lsp + QN * a.n_split) - smem) <= smem_bytes;
-    for (int t = threadIdx.x; t < QN * a.n_split; t += blockDim.x) {
-      const int q = t / a.n_split, sp = t % a.n_split, i = q / G, gg = q % G;
+    float* lsp = pst + (staged ? (size_t)QN * nsplit * HD : 0);   // [QN][n_split] split sums
+    const bool lsm = (size_t)((unsigned char*)(lsp + QN * nsplit) - smem) <= smem_bytes;
+    for (int t = threadIdx.x; t < QN * nsplit; t += blockDim.x) {
+      const int q = t / nsplit, sp = t % nsplit, i = q / G, gg = q % G;
       const size_t pi = ((size_t)(b * a.R + i) * a.nq + kvh * G + gg) * a.n_split + sp;
       const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + pi);
       wts[t] = ml.x;
@@ -455,35 +527,35 @@ struct AttnTc {
       const int i = q / G, gg = q % G;
       const size_t base_i = ((size_t)(b * a.R + i) * a.nq + kvh * G + gg) * a.n_split;
       float M = -INFINITY;
-      for (int sp = 0; sp < a.n_split; ++sp) M = fmaxf(M, wts[q * a.n_split + sp]);
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, wts[q * nsplit + sp]);
       float L = 0.f;
-      for (int sp = 0; sp < a.n_split; ++sp) {
-        const float ms = wts[q * a.n_split + sp];
+      for (int sp = 0; sp < nsplit; ++sp) {
+        const float ms = wts[q * nsplit + sp];
         const float w = ms == -INFINITY ? 0.f : __expf(ms - M);
-        wts[q * a.n_split + sp] = w;
-        L += (lsm ? lsp[q * a.n_split + sp] : __ldcg(a.part_ml + (base_i + sp) * 2 + 1)) * w;
+        wts[q * nsplit + sp] = w;
+        L += (lsm ? lsp[q * nsplit + sp] : __ldcg(a.part_ml + (base_i + sp) * 2 + 1)) * w;
       }
       const float inv = L > 0.f ? 1.f / L : 0.f;
-      for (int sp = 0; sp < a.n_split; ++sp) wts[q * a.n_split + sp] *= inv;
+      for (int sp = 0; sp < nsplit; ++sp) wts[q * nsplit + sp] *= inv;
     }
     if (staged) cp_async_wait<0>();
     __syncthreads();
     for (int t = threadIdx.x; t < QN * HD; t += blockDim.x) {
       const int q = t / HD, d = t % HD, i = q / G, gg = q % G;
       const int m = b * a.R + i, h = kvh * G + gg;
-      const float* w = wts + q * a.n_split;
+      const float* w = wts + q * nsplit;
       float acc0 = 0.f, acc1 = 0.f;
       if (staged) {
-        const float* po = pst + (size_t)q * a.n_split * HD + d;
+        const float* po = pst + (size_t)q * nsplit * HD + d;
         int sp = 0;
-        for (; sp + 2 <= a.n_split; sp += 2) {
+        for (; sp + 2 <= nsplit; sp += 2) {
           acc0 = fmaf(w[sp], po[(size_t)sp * HD], acc0);
           acc1 = fmaf(w[sp + 1], po[(size_t)(sp + 1) * HD], acc1);
         }
-        if (sp < a.n_split) acc0 = fmaf(w[sp], po[(size_t)sp * HD], acc0);
+        if (sp < nsplit) acc0 = fmaf(w[sp], po[(size_t)sp * HD], acc0);
       } else {
         const float* po = a.part_o + ((size_t)m * a.nq + h) * a.n_split * HD + d;
-        for (int sp = 0; sp < a.n_split; ++sp) acc0 = fmaf(w[sp], __ldcg(po + (size_t)sp * HD), acc0);
+        for (int sp = 0; sp < nsplit; ++sp) acc0 = fmaf(w[sp], __ldcg(po + (size_t)sp * HD), acc0);
       }
       a.out[(size_t)m * a.nq * HD + h * HD + d] = acc0 + acc1;
     }
