@@ -266,6 +266,21 @@ struct AttnTc {
       return k;
     };
     const long long q0 = begin(cta), q1 = begin(cta + 1);
+    // pages do not depend on the previous kernel: pull this CTA's K and V
+    // planes towards L2 (one bulk prefetch per 16 KB plane) before the wait
+    {
+      const __nv_bfloat16* base = (const __nv_bfloat16*)a.pool + (size_t)a.layer * a.layer_elems;
+      for (long long i = q0 * 2 + threadIdx.x; i < q1 * 2; i += blockDim.x) {
+        const long long q = i >> 1;
+        int bb = 0;
+        while (bb + 1 < B && s_off[bb + 1] <= q) ++bb;
+        const int np = s_np[bb], kvh = (int)((q - s_off[bb]) / np);
+        const int p = (int)(q - s_off[bb] - (long long)kvh * np);
+        const int pg = a.block_table[(size_t)a.seq_ids[bb] * a.max_pages + p];
+        if (pg >= 0 && pg < a.n_pages)
+          prefetch_l2_bulk(base + (((size_t)pg * 2 + (int)(i & 1)) * nkv + kvh) * PAGE * HD, PAGE * HD * 2);
+      }
+    }
     int b = 0;
     for (long long q = q0; q < q1;) {
       // sequence of flattened page q: the first b with s_off[b + 1] > q
@@ -554,8 +569,19 @@ struct AttnTc {
         }
         if (sp < nsplit) acc0 = fmaf(w[sp], po[(size_t)sp * HD], acc0);
       } else {
+        // 8 splits' loads in flight at a time; even splits to acc0 and odd
+        // ones to acc1 in order, as in the staged branch
         const float* po = a.part_o + ((size_t)m * a.nq + h) * a.n_split * HD + d;
-        for (int sp = 0; sp < nsplit; ++sp) acc0 = fmaf(w[sp], __ldcg(po + (size_t)sp * HD), acc0);
+        for (int sp = 0; sp < nsplit; sp += 8) {
+          float u[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) u[i] = __ldcg(po + (size_t)min(sp + i, nsplit - 1) * HD);
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            if (sp + i < nsplit) acc0 = fmaf(w[sp + i], u[i], acc0);
+            if (sp + i + 1 < nsplit) acc1 = fmaf(w[sp + i + 1], u[i + 1], acc1);
+          }
+        }
       }
       a.out[(size_t)m * a.nq * HD + h * HD + d] = acc0 + acc1;
     }
