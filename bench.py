@@ -166,11 +166,11 @@ def greedy_reference(eng, ids, w, n_tokens):
 def roofline_kernel_name(w):
     """The projection kernel the verify pass of this workload runs."""
     t = w.target
-    if t.wdtype == configs.BF16 and w.M > 8:
-        return "wide_kernel (tcgen05 weight-streaming projection; each launch with its wide_prep_kernel)"
+    if t.wdtype in (configs.BF16, configs.Q4_0) and w.M > 8:
+        return "wide_kernel (tcgen05 weight-streaming projection%s; each launch with its wide_prep_kernel)" % (
+            ", Q4_0 dequantised in shared memory" if t.wdtype == configs.Q4_0 else "")
     if t.wdtype in (configs.BF16, configs.Q4_0):
-        return "gemv_tc_kernel (mma.sync weight-streaming projection%s)" % (
-            ", in passes of 8 rows" if w.M > 8 else "")
+        return "gemv_tc_kernel (mma.sync weight-streaming projection)"
     return "gemv_kernel (CUDA-core weight-streaming projection)"
 
 

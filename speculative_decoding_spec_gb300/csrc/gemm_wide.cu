@@ -58,12 +58,15 @@ namespace wide {
 
 constexpr int TM = 128;              // weight rows per tile (MMA M)
 constexpr int KC = 64;               // K columns per stage (one 128-byte swizzle row of bf16)
-constexpr int NTHR = 192;            // 6 warps
+constexpr int NTHR = 192;            // 6 warps (bf16 weights)
+constexpr int NTHR_Q4 = 320;         // + 4 dequantising warps (Q4_0 weights)
 constexpr int EPI0 = 64;             // first epilogue thread
+constexpr int DQ0 = 192;             // first dequantising thread (Q4_0)
+constexpr int CODE_BYTES = TM * KC / 2;  // 4 KB of Q4_0 codes per stage
 constexpr int W_BYTES = TM * KC * 2; // 16 KB weight tile per stage
 constexpr int XCH_LD = TM + 1;       // exchange buffer row stride (floats): conflict-free both ways
 constexpr int MAX_STAGES = 8;
-constexpr int NBARS = 2 * MAX_STAGES + 6;  // full, empty, 2 acc-full, 2 acc-empty, drain, pad to 16 bytes
+constexpr int NBARS = 3 * MAX_STAGES + 6;  // full, empty, weights-ready, 2 acc-full, 2 acc-empty, drain, pad
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr unsigned SPIN_LIMIT = 1u << 26;
 constexpr int TMEM_COLS = 512;       // 2 accumulator sets x 2 chains x (hi, lo) x up to 64 columns
@@ -78,6 +81,10 @@ struct Plan {
   int map;
   int stages;
   int stage_bytes;
+  int x_off;     // activation planes within a stage
+  int c_off;     // Q4_0 codes within a stage (after the two dequantised weight planes)
+  int tx_bytes;  // bytes the TMA loads of one stage bring
+  int q4;        // Q4_0 weights, dequantised in shared memory
   int smem;      // dynamic shared memory requested (includes 1 KB alignment slack)
 };
 
@@ -192,7 +199,7 @@ struct SegIter {
 
 // ---- one CTA ----------------------------------------------------------------
 
-template <int MP>
+template <int MP, bool Q4>
 struct Cta {
   const GemvArgs& a;
   const Plan& p;
@@ -205,7 +212,7 @@ struct Cta {
   unsigned long long* trace;
   unsigned char* stages;   // p.stages x p.stage_bytes, 1024-byte aligned
   float* xch;              // [MP][XCH_LD]
-  uint64_t *full, *empty, *accf, *acce, *drain;
+  uint64_t *full, *empty, *wready, *accf, *acce, *drain;
   float* rms_s;            // [64]
   float* rope_s;           // MAP_ROPE: [M][128] the rows' RoPE (cos, sin) pairs
   int *pos_s, *page_s;     // MAP_ROPE: [64] each row's position and cache page
@@ -219,6 +226,17 @@ struct Cta {
 
   SPEC_DEV void load_w(int s, int u) const {
     const int t = u / p.C, x = (u - t * p.C) * KC;
+    if (Q4) {
+      // 128 rows x 32 code bytes (64 values); the planes are built from them
+      unsigned char* dst = stage(s) + p.c_off;
+      if (p.map == MAP_PAIR) {
+        tma_load_2d(dst, tmw, x / 2, t * 64, &full[s]);
+        tma_load_2d(dst + CODE_BYTES / 2, tmw, x / 2, a.geglu_half + t * 64, &full[s]);
+      } else {
+        tma_load_2d(dst, tmw, x / 2, t * TM, &full[s]);
+      }
+      return;
+    }
     unsigned char* dst = stage(s);
     if (p.map == MAP_PAIR) {
       // rows 0-63: gate rows 64t.., rows 64-127: the matching up rows
@@ -230,14 +248,14 @@ struct Cta {
   }
   SPEC_DEV void load_x(int s, int u) const {
     const int t = u / p.C, x = (u - t * p.C) * KC;
-    tma_load_2d(stage(s) + W_BYTES, tmx, x, 0, &full[s]);
+    tma_load_2d(stage(s) + p.x_off, tmx, x, 0, &full[s]);
   }
 
   // warp 0, one thread
   SPEC_DEV void producer() {
     const int nu = u1 - u0, pre = min(nu, p.stages);
     for (int n = 0; n < pre; ++n) {
-      mbar_expect_tx(&full[n], (unsigned)p.stage_bytes);
+      mbar_expect_tx(&full[n], (unsigned)p.tx_bytes);
       load_w(n, u0 + n);
     }
     grid_dep_wait();  // the activation planes come from the preparation kernel
@@ -247,7 +265,7 @@ struct Cta {
     for (int n = pre; n < nu; ++n) {
       const int s = n % p.stages;
       if (!wait_phase(&empty[s], ((n / p.stages) - 1) & 1, abort_s, err)) break;
-      mbar_expect_tx(&full[s], (unsigned)p.stage_bytes);
+      mbar_expect_tx(&full[s], (unsigned)p.tx_bytes);
       load_w(s, u0 + n);
       load_x(s, u0 + n);
       issued = n + 1;
@@ -269,17 +287,29 @@ struct Cta {
       const uint32_t d = tmem + (uint32_t)(acc * SET_COLS);
       for (int c = c0; c < c1; ++c, ++n) {
         const int s = n % p.stages;
-        if (!wait_phase(&full[s], (n / p.stages) & 1, abort_s, err)) {
+        if (!wait_phase(&full[s], (n / p.stages) & 1, abort_s, err) ||
+            (Q4 && !wait_phase(&wready[s], (n / p.stages) & 1, abort_s, err))) {
           ok = false;
           break;
         }
         if (n == 0) stamp(trace, 3);
         fence_after();
-        const uint32_t w = sa(stage(s)), x = w + W_BYTES;
+        const uint32_t w = sa(stage(s)), x = w + (uint32_t)p.x_off;
+        if (Q4) {
+          // hi weight plane into chain 0, lo plane into chain 1
 #pragma unroll
-        for (int ks = 0; ks < KC / 16; ++ks)
-          mma_bf16(d + (uint32_t)((ks & 1) * CHAIN_COLS), sw128_desc(w + 32 * ks), sw128_desc(x + 32 * ks), idesc,
-                   (c > c0 || ks > 1) ? 1u : 0u);
+          for (int ks = 0; ks < KC / 16; ++ks) {
+            const uint64_t xd = sw128_desc(x + 32 * ks);
+            const uint32_t acc = (c > c0 || ks > 0) ? 1u : 0u;
+            mma_bf16(d, sw128_desc(w + 32 * ks), xd, idesc, acc);
+            mma_bf16(d + (uint32_t)CHAIN_COLS, sw128_desc(w + W_BYTES + 32 * ks), xd, idesc, acc);
+          }
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < KC / 16; ++ks)
+            mma_bf16(d + (uint32_t)((ks & 1) * CHAIN_COLS), sw128_desc(w + 32 * ks), sw128_desc(x + 32 * ks), idesc,
+                     (c > c0 || ks > 1) ? 1u : 0u);
+        }
         mma_commit(&empty[s]);
       }
       if (!ok) break;
@@ -290,6 +320,77 @@ struct Cta {
     // every MMA of this CTA complete before its tensor memory is freed
     mma_commit(drain);
     drain_phase(drain, 0);
+  }
+
+  // warps 6-9 (Q4_0): thread r turns row r of a stage's codes into the two
+  // bf16 weight planes: w = scale * (code - 8) is exact in fp32 (an 11-bit
+  // scale times a 4-bit integer); hi = bf16(w) and lo = bf16(w - hi) hold it
+  // exactly. Rows are written in the 128-byte swizzle layout the MMA reads
+  // (16-byte chunk j of row r at chunk j ^ (r % 8)).
+  SPEC_DEV void dequant() {
+    const int r = threadIdx.x - DQ0, lane = threadIdx.x & 31;
+    const int K32 = a.K / 32, nu = u1 - u0;
+    const uint16_t* S = (const uint16_t*)a.W.scales;
+    for (int n = 0; n < nu; ++n) {
+      const int u = u0 + n, t = u / p.C, c = u - t * p.C, s = n % p.stages;
+      // this row's two block scales (zero past the matrix, whose codes read as zero)
+      int grow;
+      bool valid;
+      if (p.map == MAP_PAIR) {
+        const int j = t * 64 + (r & 63);
+        valid = j < a.geglu_half;
+        grow = (r < 64 ? 0 : a.geglu_half) + j;
+      } else {
+        grow = t * TM + r;
+        valid = grow < a.N;
+      }
+      const unsigned int sw = valid ? __ldg(reinterpret_cast<const unsigned int*>(S + (size_t)grow * K32 + 2 * c)) : 0u;
+      int ok = 1;
+      if (lane == 0) ok = wait_phase(&full[s], (n / p.stages) & 1, abort_s, err) ? 1 : 0;
+      ok = __shfl_sync(FULL, ok, 0);
+      if (!ok) break;
+      unsigned char* st = stage(s);
+      const uint4 q0 = *reinterpret_cast<const uint4*>(st + p.c_off + r * 32);
+      const uint4 q1 = *reinterpret_cast<const uint4*>(st + p.c_off + r * 32 + 16);
+      const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      unsigned char* whi = st + r * 128;
+      unsigned char* wlo = whi + W_BYTES;
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const float sc = __half2float(__ushort_as_half((unsigned short)(blk ? sw >> 16 : sw & 0xFFFFu)));
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t w0 = words[blk * 4 + half * 2], w1 = words[blk * 4 + half * 2 + 1];
+#pragma unroll
+          for (int nib = 0; nib < 2; ++nib) {
+            // values 32*blk + 16*nib + 8*half + i, i = 0..7: nibble `nib` of code byte 8*half + i
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t wd = i < 2 ? w0 : w1;
+              const int sh = 16 * (i & 1);
+              const uint32_t b0 = (wd >> sh) & 0xFFu, b1 = (wd >> (sh + 8)) & 0xFFu;
+              const int c0 = nib ? (int)(b0 >> 4) : (int)(b0 & 15u);
+              const int c1 = nib ? (int)(b1 >> 4) : (int)(b1 & 15u);
+              const float x0 = sc * (float)(c0 - 8), x1 = sc * (float)(c1 - 8);
+              const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+              const __nv_bfloat162 hh = __halves2bfloat162(h0, h1);
+              const __nv_bfloat162 ll = __floats2bfloat162_rn(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+              hi[i] = *reinterpret_cast<const uint32_t*>(&hh);
+              lo[i] = *reinterpret_cast<const uint32_t*>(&ll);
+            }
+            const int chunk = blk * 4 + nib * 2 + half;
+            const int off = ((chunk ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(whi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(wlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+      }
+      // the planes are read by the tensor cores (async proxy)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wready[s]);
+    }
   }
 
   // ---- epilogue (warps 2-5; thread r of the tile is TMEM lane r) ----
@@ -491,8 +592,8 @@ struct Cta {
   }
 };
 
-template <int MP>
-__global__ void __launch_bounds__(NTHR, 1)
+template <int MP, bool Q4>
+__global__ void __launch_bounds__(Q4 ? NTHR_Q4 : NTHR, 1)
     wide_kernel(const __grid_constant__ GemvArgs a, const __grid_constant__ Plan p,
                 const __grid_constant__ CUtensorMap tmw,
                 const __grid_constant__ CUtensorMap tmx, const float* inv_rms, float* fix, unsigned int* cnt,
@@ -500,14 +601,15 @@ __global__ void __launch_bounds__(NTHR, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t mis = sa(smem_raw) & 1023u;
   unsigned char* base = smem_raw + (mis ? 1024 - mis : 0);
-  Cta<MP> k{a, p, &tmw, &tmx, inv_rms, fix, cnt, err, a.wide.trace};
+  Cta<MP, Q4> k{a, p, &tmw, &tmx, inv_rms, fix, cnt, err, a.wide.trace};
   if (threadIdx.x == 0) stamp(k.trace, 0);
   k.stages = base;
   k.xch = reinterpret_cast<float*>(base + (size_t)p.stages * p.stage_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(k.xch + MP * XCH_LD);
   k.full = bars;
   k.empty = bars + MAX_STAGES;
-  k.accf = bars + 2 * MAX_STAGES;
+  k.wready = bars + 2 * MAX_STAGES;
+  k.accf = bars + 3 * MAX_STAGES;
   k.acce = k.accf + 2;
   k.drain = k.acce + 2;
   k.rms_s = reinterpret_cast<float*>(bars + NBARS);
@@ -526,6 +628,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&k.full[s], 1);
       mbar_init(&k.empty[s], 1);
+      mbar_init(&k.wready[s], 4);  // one arrival per dequantising warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&k.accf[i], 1);
@@ -553,8 +656,10 @@ __global__ void __launch_bounds__(NTHR, 1)
   } else if (warp == 1) {
     if (lane == 0) k.mma_loop();
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     k.epilogue();
+  } else if (Q4) {
+    k.dequant();
   }
   fence_before();
   __syncthreads();
@@ -656,6 +761,19 @@ bool encode(CUtensorMap* m, const void* base, int inner, int rows, int box_rows)
 
 // shared memory besides the stages: exchange tile, barriers, per-row tables,
 // the RoPE rows (RoPE epilogue only), tensor-memory slot, flags, 1 KB alignment
+// Q4_0 codes [rows][inner bytes] as a 2-D uint8 tensor, boxes of box_rows x
+// 32 bytes (64 values), no swizzle.
+bool encode_codes(CUtensorMap* m, const void* base, int inner, int rows, int box_rows) {
+  if (!g_encode || ((uintptr_t)base & 15) || inner % 16) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)inner};
+  const cuuint32_t box[2] = {(cuuint32_t)(KC / 2), (cuuint32_t)box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t fixed_smem(int MP, bool rope) {
   return (size_t)MP * XCH_LD * 4 + NBARS * 8 + 3 * 64 * 4 + (rope ? (size_t)MP * TM * 4 : 0) + 4 + 4 + 16 + 1024;
 }
@@ -663,8 +781,10 @@ size_t fixed_smem(int MP, bool rope) {
 template <int MP>
 cudaError_t launch_mp(const cudaLaunchConfig_t& cfg, const GemvArgs& a, const Plan& p, const CUtensorMap& tmw,
                       const CUtensorMap& tmx) {
-  return cudaLaunchKernelEx(&cfg, wide_kernel<MP>, a, p, tmw, tmx, (const float*)a.wide.rms, a.wide.fix, a.tc_cnt,
-                            a.wide.err);
+  return p.q4 ? cudaLaunchKernelEx(&cfg, wide_kernel<MP, true>, a, p, tmw, tmx, (const float*)a.wide.rms, a.wide.fix,
+                                   a.tc_cnt, a.wide.err)
+              : cudaLaunchKernelEx(&cfg, wide_kernel<MP, false>, a, p, tmw, tmx, (const float*)a.wide.rms, a.wide.fix,
+                                   a.tc_cnt, a.wide.err);
 }
 
 }  // namespace
@@ -679,7 +799,22 @@ bool make_plan(const GemvArgs& a, int nsm, Plan& p) {
   p.U = p.T * p.C;
   p.grid = std::min(p.U, nsm);
   p.MP = (a.M + 15) / 16 * 16;
-  p.stage_bytes = W_BYTES + 2 * p.MP * KC * 2;
+  p.q4 = a.W.dtype == DT_Q4_0;
+  if (p.q4 && !a.W.scales) return false;
+  const int xbytes = 2 * p.MP * KC * 2;
+  if (p.q4) {
+    // [hi plane | lo plane | activation planes | codes]
+    p.x_off = 2 * W_BYTES;
+    p.c_off = 2 * W_BYTES + xbytes;
+    p.stage_bytes = 2 * W_BYTES + xbytes + CODE_BYTES;
+    p.tx_bytes = xbytes + CODE_BYTES;
+  } else {
+    // [weights | activation planes]
+    p.x_off = W_BYTES;
+    p.c_off = 0;
+    p.stage_bytes = W_BYTES + xbytes;
+    p.tx_bytes = p.stage_bytes;
+  }
   const size_t fixed = fixed_smem(p.MP, p.map == MAP_ROPE);
   p.stages = (int)std::min<size_t>(MAX_STAGES, (SMEM_LIMIT - fixed) / p.stage_bytes);
   if (p.stages < 2) return false;
@@ -692,18 +827,22 @@ bool make_plan(const GemvArgs& a, int nsm, Plan& p) {
 using namespace wide;
 
 void setup_gemv_wide_attributes() {
-  cudaFuncSetAttribute(wide_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
-  cudaFuncSetAttribute(wide_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
-  cudaFuncSetAttribute(wide_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
-  cudaFuncSetAttribute(wide_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<48, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<48, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
+  cudaFuncSetAttribute(wide_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT);
 }
 
 size_t gemv_wide_fix_bytes() { return (size_t)num_sms() * 2 * 64 * TM * sizeof(float); }
 
 bool gemv_wide_ok(const GemvArgs& a) {
   Plan p;
-  return a.W.dtype == DT_BF16 && a.wide.xs && a.wide.rms && a.wide.fix && a.tc_cnt && a.K <= a.wide.kmax &&
-         make_plan(a, num_sms(), p);
+  return (a.W.dtype == DT_BF16 || a.W.dtype == DT_Q4_0) && a.wide.xs && a.wide.rms && a.wide.fix && a.tc_cnt &&
+         a.K <= a.wide.kmax && make_plan(a, num_sms(), p);
 }
 
 // M in 1..64 rows, bf16 weights, K % 64 == 0 (gemv_wide_ok). Launches the
@@ -713,9 +852,9 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
   Plan p;
   if (!make_plan(a, num_sms(), p)) return -1;
   CUtensorMap tmw, tmx;
-  if (!encode(&tmw, a.W.data, a.K, a.N, p.map == MAP_PAIR ? 64 : TM) ||
-      !encode(&tmx, a.wide.xs, a.K, 2 * p.MP, 2 * p.MP))
-    return -1;
+  const int box_rows = p.map == MAP_PAIR ? 64 : TM;
+  const bool wok = p.q4 ? encode_codes(&tmw, a.W.data, a.K / 2, a.N, box_rows) : encode(&tmw, a.W.data, a.K, a.N, box_rows);
+  if (!wok || !encode(&tmx, a.wide.xs, a.K, 2 * p.MP, 2 * p.MP)) return -1;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -730,7 +869,7 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
     return -1;
   cudaLaunchConfig_t cfg = pc;
   cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(NTHR);
+  cfg.blockDim = dim3(p.q4 ? NTHR_Q4 : NTHR);
   cfg.dynamicSmemBytes = p.smem;
   cudaError_t e;
   switch (p.MP) {

@@ -76,12 +76,13 @@ def test_linear_rows_do_not_depend_on_M():
         assert torch.equal(part, full[:M])
 
 
-def test_wide_rows_do_not_depend_on_M():
-    """Above 8 rows (bf16) the projection runs on tcgen05 with the rows padded
-    to a multiple of 16; a row's result is bitwise the same for every row
-    count of that path, so a batch's verify rows do not depend on the batch."""
+@pytest.mark.parametrize("dtype", [configs.BF16, configs.Q4_0])
+def test_wide_rows_do_not_depend_on_M(dtype):
+    """Above 8 rows the projection runs on tcgen05 with the rows padded to a
+    multiple of 16; a row's result is bitwise the same for every row count of
+    that path, so a batch's verify rows do not depend on the batch."""
     g = torch.Generator(device="cuda").manual_seed(6)
-    w = synth.make_matrix(g, configs.BF16, 1, 1000, 1536, 0.02, "cuda")
+    w = synth.make_matrix(g, dtype, 1, 1000, 1536, 0.02, "cuda")
     x = _x(64, 1536, 10)
     full = binding.spec_linear(w, x)
     for M in (9, 16, 17, 33, 40, 48):
