@@ -33,7 +33,9 @@
 // The activations enter as bf16 hi + lo planes (x = hi + lo to 2^-17), written
 // once per launch by a small preparation kernel that also applies the RMSNorm
 // gain and computes each row's 1/rms; so a result equals an fp32-activation dot
-// product of the bf16 weights, as in the register-fragment kernel.
+// product of the bf16 weights, as in the register-fragment kernel. Q4_0
+// weights: four more warps expand each stage's codes and block scales into
+// fp16 hi + lo weight planes (exact), and the activation planes are fp16.
 //
 // Work split: units are (tile, 64-column chunk) pairs in tile-major order and
 // CTA b owns the balanced range [U*b/G, U*(b+1)/G). A tile cut between CTAs is
@@ -106,6 +108,10 @@ SPEC_DEV uint64_t sw128_desc(uint32_t saddr) {
 // bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// The same with fp16 A and B (type fields 0).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 SPEC_DEV void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
@@ -276,7 +282,7 @@ struct Cta {
 
   // warp 1, one thread
   SPEC_DEV void mma_loop() {
-    const uint32_t idesc = idesc_bf16(TM, 2 * MP);
+    const uint32_t idesc = Q4 ? idesc_f16(TM, 2 * MP) : idesc_bf16(TM, 2 * MP);
     SegIter it{u0, u1, p.C};
     int t, c0, c1, n = 0, i = 0;
     bool ok = true;
@@ -322,15 +328,18 @@ struct Cta {
     drain_phase(drain, 0);
   }
 
-  // warps 6-9 (Q4_0): thread r turns row r of a stage's codes into the two
-  // bf16 weight planes: w = scale * (code - 8) is exact in fp32 (an 11-bit
-  // scale times a 4-bit integer); hi = bf16(w) and lo = bf16(w - hi) hold it
-  // exactly. Rows are written in the 128-byte swizzle layout the MMA reads
+  // warps 6-9 (Q4_0): thread r turns row r of a stage's codes into two fp16
+  // weight planes with packed half2 arithmetic: 0x6400 | code is the fp16
+  // 1024 + code, so subtracting 1032 leaves code - 8 exactly; hi = (code - 8)
+  // * scale rounded and lo = fma(code - 8, scale, -hi), the exact remainder
+  // (an 11-bit scale times a 4-bit integer; exact for every normal fp16
+  // scale). Rows are written in the 128-byte swizzle layout the MMA reads
   // (16-byte chunk j of row r at chunk j ^ (r % 8)).
   SPEC_DEV void dequant() {
     const int r = threadIdx.x - DQ0, lane = threadIdx.x & 31;
     const int K32 = a.K / 32, nu = u1 - u0;
     const uint16_t* S = (const uint16_t*)a.W.scales;
+    const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
     for (int n = 0; n < nu; ++n) {
       const int u = u0 + n, t = u / p.C, c = u - t * p.C, s = n % p.stages;
       // this row's two block scales (zero past the matrix, whose codes read as zero)
@@ -357,32 +366,29 @@ struct Cta {
       unsigned char* wlo = whi + W_BYTES;
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
-        const float sc = __half2float(__ushort_as_half((unsigned short)(blk ? sw >> 16 : sw & 0xFFFFu)));
+        const __half2 s2 = __half2half2(__ushort_as_half((unsigned short)(blk ? sw >> 16 : sw & 0xFFFFu)));
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const uint32_t w0 = words[blk * 4 + half * 2], w1 = words[blk * 4 + half * 2 + 1];
 #pragma unroll
           for (int nib = 0; nib < 2; ++nib) {
             // values 32*blk + 16*nib + 8*half + i, i = 0..7: nibble `nib` of code byte 8*half + i
+            const uint32_t n0 = (nib ? w0 >> 4 : w0) & 0x0F0F0F0Fu, n1 = (nib ? w1 >> 4 : w1) & 0x0F0F0F0Fu;
+            const uint32_t e[4] = {__byte_perm(n0, 0x6464u, 0x5140), __byte_perm(n0, 0x6464u, 0x5342),
+                                   __byte_perm(n1, 0x6464u, 0x5140), __byte_perm(n1, 0x6464u, 0x5342)};
             uint32_t hi[4], lo[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint32_t wd = i < 2 ? w0 : w1;
-              const int sh = 16 * (i & 1);
-              const uint32_t b0 = (wd >> sh) & 0xFFu, b1 = (wd >> (sh + 8)) & 0xFFu;
-              const int c0 = nib ? (int)(b0 >> 4) : (int)(b0 & 15u);
-              const int c1 = nib ? (int)(b1 >> 4) : (int)(b1 & 15u);
-              const float x0 = sc * (float)(c0 - 8), x1 = sc * (float)(c1 - 8);
-              const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-              const __nv_bfloat162 hh = __halves2bfloat162(h0, h1);
-              const __nv_bfloat162 ll = __floats2bfloat162_rn(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
-              hi[i] = *reinterpret_cast<const uint32_t*>(&hh);
-              lo[i] = *reinterpret_cast<const uint32_t*>(&ll);
+              const __half2 cv = __hsub2(*reinterpret_cast<const __half2*>(&e[i]), off);
+              const __half2 h = __hmul2(cv, s2);
+              const __half2 l = __hfma2(cv, s2, __hneg2(h));
+              hi[i] = *reinterpret_cast<const uint32_t*>(&h);
+              lo[i] = *reinterpret_cast<const uint32_t*>(&l);
             }
             const int chunk = blk * 4 + nib * 2 + half;
-            const int off = ((chunk ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(whi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(wlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            const int offc = ((chunk ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(whi + offc) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(wlo + offc) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
         }
       }
@@ -680,10 +686,10 @@ __global__ void __launch_bounds__(Q4 ? NTHR_Q4 : NTHR, 1)
   run_tail(a.tail);
 }
 
-// Activation rows -> bf16 hi/lo planes [2][MP][K] (gain applied) and 1/rms
+// Activation rows -> bf16 (f16: fp16) hi/lo planes [2][MP][K] (gain applied) and 1/rms
 // per row (1 without a gain, 0 for the padding rows, whose planes are zero).
 __global__ void __launch_bounds__(256) wide_prep_kernel(const float* X, int ldx, int M, int K, const float* gain,
-                                                        float eps, int MP, uint16_t* xs, float* rms) {
+                                                        float eps, int MP, uint16_t* xs, float* rms, int f16) {
   __shared__ float red[32];
   const int m = blockIdx.x;
   grid_dep_wait();
@@ -713,12 +719,20 @@ __global__ void __launch_bounds__(256) wide_prep_kernel(const float* X, int ldx,
     uint32_t h[4], l[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
-      const __nv_bfloat162 hh = __halves2bfloat162(h0, h1);
-      const __nv_bfloat162 ll =
-          __floats2bfloat162_rn(v[2 * i] - __bfloat162float(h0), v[2 * i + 1] - __bfloat162float(h1));
-      h[i] = *reinterpret_cast<const uint32_t*>(&hh);
-      l[i] = *reinterpret_cast<const uint32_t*>(&ll);
+      if (f16) {
+        const __half h0 = __float2half_rn(v[2 * i]), h1 = __float2half_rn(v[2 * i + 1]);
+        const __half2 hh = __halves2half2(h0, h1);
+        const __half2 ll = __floats2half2_rn(v[2 * i] - __half2float(h0), v[2 * i + 1] - __half2float(h1));
+        h[i] = *reinterpret_cast<const uint32_t*>(&hh);
+        l[i] = *reinterpret_cast<const uint32_t*>(&ll);
+      } else {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * i]), h1 = __float2bfloat16_rn(v[2 * i + 1]);
+        const __nv_bfloat162 hh = __halves2bfloat162(h0, h1);
+        const __nv_bfloat162 ll =
+            __floats2bfloat162_rn(v[2 * i] - __bfloat162float(h0), v[2 * i + 1] - __bfloat162float(h1));
+        h[i] = *reinterpret_cast<const uint32_t*>(&hh);
+        l[i] = *reinterpret_cast<const uint32_t*>(&ll);
+      }
     }
     *reinterpret_cast<uint4*>(hi + c8) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(lo + c8) = make_uint4(l[0], l[1], l[2], l[3]);
@@ -864,8 +878,8 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
   pc.stream = st;
   pc.attrs = attr;
   pc.numAttrs = a.pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&pc, wide_prep_kernel, a.X, a.ldx, a.M, a.K, a.gain, a.eps, p.MP, a.wide.xs, a.wide.rms) !=
-      cudaSuccess)
+  if (cudaLaunchKernelEx(&pc, wide_prep_kernel, a.X, a.ldx, a.M, a.K, a.gain, a.eps, p.MP, a.wide.xs, a.wide.rms,
+                         p.q4) != cudaSuccess)
     return -1;
   cudaLaunchConfig_t cfg = pc;
   cfg.gridDim = dim3(p.grid);
