@@ -49,6 +49,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
 
 #include "common.cuh"
@@ -87,6 +88,7 @@ struct Plan {
   int c_off;     // Q4_0 codes within a stage (after the two dequantised weight planes)
   int tx_bytes;  // bytes the TMA loads of one stage bring
   int q4;        // Q4_0 weights, dequantised in shared memory
+  int S;         // CTAs per tile in a thread-block cluster (1: balanced unit ranges, global fixups)
   int smem;      // dynamic shared memory requested (includes 1 KB alignment slack)
 };
 
@@ -155,6 +157,24 @@ SPEC_DEV void stamp(unsigned long long* tr, int i) {
   if (tr) tr[blockIdx.x * 16 + i] = globaltimer();
 }
 
+// Thread-block cluster: barrier over every thread of every CTA, this CTA's
+// rank, and a load from the shared memory of CTA `rank` of the cluster.
+SPEC_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+SPEC_DEV unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+SPEC_DEV float ld_peer(const float* p, unsigned rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(sa(p)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
 // Named barrier of the 4 epilogue warps.
 SPEC_DEV void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -178,7 +198,13 @@ SPEC_DEV void drain_phase(uint64_t* b, unsigned parity) {
 
 // ---- plan ----------------------------------------------------------------
 
-__host__ __device__ inline int unit_begin(int b, const Plan& p) { return (int)(((long long)b * p.U) / p.grid); }
+// First unit of CTA b. Cluster mode (S > 1): cluster t = b / S takes tile t,
+// its CTA j the chunks [C*j/S, C*(j+1)/S). Otherwise balanced ranges of the
+// tile-major unit list.
+__host__ __device__ inline int unit_begin(int b, const Plan& p) {
+  if (p.S > 1) return (b / p.S) * p.C + (p.C * (b % p.S)) / p.S;
+  return (int)(((long long)b * p.U) / p.grid);
+}
 
 // CTA whose unit range holds unit u.
 __host__ __device__ inline int cta_of(int u, const Plan& p) {
@@ -413,39 +439,69 @@ struct Cta {
 #pragma unroll
     for (int m = 0; m < MP; ++m) xch[m * XCH_LD + r] = v[m] * rms_s[m];
     epi_sync();
-    if (p.map == MAP_ROPE) rope(t, r);
-    else if (p.map == MAP_PAIR) geglu(t, e);
-    else if (a.epi == EPI_ARGMAX) argmax(t, r, e, mybest);
-    else store_add(t, r);
+    finish_rows(t, 0, a.M, mybest);
     epi_sync();  // xch is free for the next tile
   }
 
-  SPEC_DEV void store_add(int t, int r) {
+  // The operation's epilogue for activation rows [m0, m1) of the tile in xch.
+  SPEC_DEV void finish_rows(int t, int m0, int m1, unsigned long long& mybest) {
+    const int r = row(), e = threadIdx.x - EPI0;
+    if (p.map == MAP_ROPE) rope(t, r, m0, m1);
+    else if (p.map == MAP_PAIR) geglu(t, e, m0, m1);
+    else if (a.epi == EPI_ARGMAX) argmax(t, r, e, m0, m1, mybest);
+    else store_add(t, r, m0, m1);
+  }
+
+  // Cluster mode: each CTA of the cluster holds its K-range's partial tile in
+  // xch (unscaled); CTA `rank` sums activation rows [M*rank/S, M*(rank+1)/S)
+  // over the cluster's CTAs in rank order (distributed shared memory), scales
+  // them and finishes those rows.
+  SPEC_DEV void cluster_finish() {
+    const int S = p.S, rank = (int)cluster_rank(), t = blockIdx.x / S, r = row();
+    const int m0 = (a.M * rank) / S, m1 = (a.M * (rank + 1)) / S;
+    if (threadIdx.x == EPI0) stamp(trace, 9);
+    for (int m = m0; m < m1; ++m) {
+      float u[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) u[j] = ld_peer(xch + m * XCH_LD + r, (unsigned)min(j, S - 1));
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc += j < S ? u[j] : 0.f;
+      xch[m * XCH_LD + r] = acc * rms_s[m];
+    }
+    epi_sync();
+    if (threadIdx.x == EPI0) stamp(trace, 10);
+    unsigned long long unused = 0ull;
+    finish_rows(t, m0, m1, unused);
+    if (threadIdx.x == EPI0) stamp(trace, 11);
+  }
+
+  SPEC_DEV void store_add(int t, int r, int ma, int mb) {
     const int n = t * TM + r;
     if (n >= a.N) return;
     if (a.epi == EPI_ADD) {
       // residual add, 32 rows at a time with the reads ahead of the writes
-      for (int m0 = 0; m0 < a.M; m0 += 32) {
+      for (int m0 = ma; m0 < mb; m0 += 32) {
         float old[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) old[i] = __ldcg(a.Y + (size_t)min(m0 + i, a.M - 1) * a.ldy + n);
+        for (int i = 0; i < 32; ++i) old[i] = __ldcg(a.Y + (size_t)min(m0 + i, mb - 1) * a.ldy + n);
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (m0 + i < a.M) a.Y[(size_t)(m0 + i) * a.ldy + n] = old[i] + xch[(m0 + i) * XCH_LD + r];
+          if (m0 + i < mb) a.Y[(size_t)(m0 + i) * a.ldy + n] = old[i] + xch[(m0 + i) * XCH_LD + r];
       }
       return;
     }
 #pragma unroll 4
-    for (int m = 0; m < a.M; ++m) a.Y[(size_t)m * a.ldy + n] = xch[m * XCH_LD + r];
+    for (int m = ma; m < mb; ++m) a.Y[(size_t)m * a.ldy + n] = xch[m * XCH_LD + r];
   }
 
-  SPEC_DEV void argmax(int t, int r, int e, unsigned long long& mybest) {
+  SPEC_DEV void argmax(int t, int r, int e, int ma, int mb, unsigned long long& mybest) {
     const int n = t * TM + r;
     if (a.Y && n < a.N) {
 #pragma unroll 4
-      for (int m = 0; m < a.M; ++m) a.Y[(size_t)m * a.ldy + n] = xch[m * XCH_LD + r];
+      for (int m = ma; m < mb; ++m) a.Y[(size_t)m * a.ldy + n] = xch[m * XCH_LD + r];
     }
-    if (e < a.M) {
+    if (e >= ma && e < mb) {
       const int nv = min(TM, a.N - t * TM);
       for (int j = 0; j < nv; ++j) {
         const unsigned long long key = pack_best(xch[e * XCH_LD + j], (uint32_t)(t * TM + j));
@@ -456,11 +512,11 @@ struct Cta {
 
   // gated GELU: tile rows 0-63 are gate rows j = 64t + c, rows 64-127 the
   // matching up rows; thread e takes column c = e % 64 of every other row
-  SPEC_DEV void geglu(int t, int e) {
+  SPEC_DEV void geglu(int t, int e, int ma, int mb) {
     const int c = e & 63, j = t * 64 + c;
     if (j >= a.geglu_half) return;
 #pragma unroll 2
-    for (int m = e >> 6; m < a.M; m += 2) {
+    for (int m = ma + (e >> 6); m < mb; m += 2) {
       const float g = xch[m * XCH_LD + c];
       const float gl = 0.5f * g * (1.f + erff(g * 0.70710678118654752f));
       a.Y[(size_t)m * a.ldy + j] = gl * xch[m * XCH_LD + 64 + c];
@@ -469,14 +525,14 @@ struct Cta {
 
   // q, k, v head t (head_dim 128): rotate-half RoPE pairs element r with
   // r +- 64; q goes to Y, k and v to the row's slot of the paged cache.
-  SPEC_DEV void rope(int t, int r) {
+  SPEC_DEV void rope(int t, int r, int ma, int mb) {
     const RopeEpi& E = a.rope;
     const int j = r & 63, h = t;
     const bool second = r >= 64, rot = h < E.nq + E.nkv, is_q = h < E.nq;
     const int plane = rot ? 0 : 1, kh = h - E.nq - plane * E.nkv;
     // the rows' tables were loaded into shared memory at the epilogue start
 #pragma unroll 4
-    for (int m = 0; m < a.M; ++m) {
+    for (int m = ma; m < mb; ++m) {
       const float self = xch[m * XCH_LD + r], part = xch[m * XCH_LD + (r ^ 64)];
       const float co = rope_s[m * TM + 2 * j], si = rope_s[m * TM + 2 * j + 1];
       const float x0 = second ? part : self, x1 = second ? self : part;
@@ -588,8 +644,18 @@ struct Cta {
       }
       fence_before();
       mbar_arrive(&acce[acc]);
-      if (c0 == 0 && c1 == p.C) finish(t, v, mybest);
-      else partial(t, i, v, mybest);
+      if (p.S > 1) {
+        // cluster mode: this CTA's partial of its one tile stays in shared
+        // memory for the cluster's reduction after the roles finish
+        const int r = row();
+#pragma unroll
+        for (int m = 0; m < MP; ++m) xch[m * XCH_LD + r] = v[m];
+        if (e == 0) stamp(trace, 8);
+      } else if (c0 == 0 && c1 == p.C) {
+        finish(t, v, mybest);
+      } else {
+        partial(t, i, v, mybest);
+      }
       if (i == 0 && e == 0) stamp(trace, 13);
       ++i;
     }
@@ -669,6 +735,12 @@ __global__ void __launch_bounds__(Q4 ? NTHR_Q4 : NTHR, 1)
   }
   fence_before();
   __syncthreads();
+  if (p.S > 1) {
+    // every CTA of the cluster passes both barriers, whatever happened above
+    cluster_sync();
+    if (warp >= 2 && warp < 6 && !*k.abort_s) k.cluster_finish();
+    cluster_sync();
+  }
   if (warp == 1) {
     fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(k.tmem), "r"(TMEM_COLS) : "memory");
@@ -792,6 +864,44 @@ size_t fixed_smem(int MP, bool rope) {
   return (size_t)MP * XCH_LD * 4 + NBARS * 8 + 3 * 64 * 4 + (rope ? (size_t)MP * TM * 4 : 0) + 4 + 4 + 16 + 1024;
 }
 
+const void* kernel_of(int MP, bool q4) {
+  switch (MP) {
+    case 16: return q4 ? (const void*)wide_kernel<16, true> : (const void*)wide_kernel<16, false>;
+    case 32: return q4 ? (const void*)wide_kernel<32, true> : (const void*)wide_kernel<32, false>;
+    case 48: return q4 ? (const void*)wide_kernel<48, true> : (const void*)wide_kernel<48, false>;
+    default: return q4 ? (const void*)wide_kernel<64, true> : (const void*)wide_kernel<64, false>;
+  }
+}
+
+// Clusters of S CTAs of this kernel and shared memory that the GPU holds at
+// once (cached).
+int max_clusters(const Plan& p) {
+  static std::mutex mu;
+  static std::map<long long, int> cache;
+  const long long key = ((long long)p.MP * 2 + p.q4) * 16 * (1 << 20) + (long long)p.S * (1 << 20) + p.smem;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.T * p.S);
+  cfg.blockDim = dim3(p.q4 ? NTHR_Q4 : NTHR);
+  cfg.dynamicSmemBytes = p.smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel_of(p.MP, p.q4), &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
+
 template <int MP>
 cudaError_t launch_mp(const cudaLaunchConfig_t& cfg, const GemvArgs& a, const Plan& p, const CUtensorMap& tmw,
                       const CUtensorMap& tmx) {
@@ -811,7 +921,11 @@ bool make_plan(const GemvArgs& a, int nsm, Plan& p) {
   p.T = p.map == MAP_PAIR ? (a.geglu_half + 63) / 64 : (a.N + TM - 1) / TM;
   p.C = a.K / KC;
   p.U = p.T * p.C;
-  p.grid = std::min(p.U, nsm);
+  // few tiles: a cluster of S CTAs per tile (reduced in distributed shared
+  // memory); the launcher lowers S until every cluster is resident at once
+  p.S = 1;
+  if (a.epi != EPI_ARGMAX && 2 * p.T <= nsm) p.S = std::min(std::min(8, nsm / p.T), p.C);
+  p.grid = p.S > 1 ? p.T * p.S : std::min(p.U, nsm);
   p.MP = (a.M + 15) / 16 * 16;
   p.q4 = a.W.dtype == DT_Q4_0;
   if (p.q4 && !a.W.scales) return false;
@@ -865,6 +979,23 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
   std::call_once(g_once, init_encode);
   Plan p;
   if (!make_plan(a, num_sms(), p)) return -1;
+  while (p.S > 1 && max_clusters(p) < p.T) --p.S;
+  // The cluster reduction removes the split-tile tail (about 10 us) but leaves
+  // nsm - T*S SMs idle: keep it only while the streaming time those SMs would
+  // have saved (the weights at about 6 TB/s) stays under about 5 us, and only
+  // for matrices of at most 64 MB (larger ones measured slower inside the
+  // pipelined pass, where a cluster waits for S free SMs of one GPC).
+  if (p.S > 1) {
+    const double wbytes = (double)a.N * a.K * (p.q4 ? 0.5625 : 2.0);
+    const double lost_us = wbytes / 6.0e6 * ((double)num_sms() / (p.T * p.S) - 1.0);
+    if (lost_us > 5.0 || wbytes > 64.0 * (1 << 20)) p.S = 1;
+  }
+  if (p.S <= 1) {
+    p.S = 1;
+    p.grid = std::min(p.U, num_sms());
+  } else {
+    p.grid = p.T * p.S;
+  }
   CUtensorMap tmw, tmx;
   const int box_rows = p.map == MAP_PAIR ? 64 : TM;
   const bool wok = p.q4 ? encode_codes(&tmw, a.W.data, a.K / 2, a.N, box_rows) : encode(&tmw, a.W.data, a.K, a.N, box_rows);
@@ -885,6 +1016,14 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
   cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(p.q4 ? NTHR_Q4 : NTHR);
   cfg.dynamicSmemBytes = p.smem;
+  cudaLaunchAttribute attr2[2];
+  attr2[0] = attr[0];
+  attr2[1].id = cudaLaunchAttributeClusterDimension;
+  attr2[1].val.clusterDim.x = p.S;
+  attr2[1].val.clusterDim.y = 1;
+  attr2[1].val.clusterDim.z = 1;
+  cfg.attrs = a.pdl ? attr2 : attr2 + 1;
+  cfg.numAttrs = (a.pdl ? 1 : 0) + (p.S > 1 ? 1 : 0);
   cudaError_t e;
   switch (p.MP) {
     case 16: e = launch_mp<16>(cfg, a, p, tmw, tmx); break;
