@@ -76,15 +76,13 @@ int attention_tc(const AttnArgs& a0, unsigned int* counters, int pps, cudaStream
   AttnArgs a = a0;
   const int QN = a.R * (a.nq / a.nkv);
   const int qt = (QN + 15) / 16;
-  // Balanced page ranges (one CTA per SM) for one-row batched calls (the
-  // drafter's cross-attention over ragged contexts), where a fixed split of the
-  // page capacity leaves long sequences with many rounds of two page slots per
-  // CTA. For verify rows (rounds of more page slots) the fixed splits measured
-  // faster: a balanced CTA that takes pieces of two pairs pays the per-split
-  // costs (queries, combine, partial) twice. The partials of a balanced launch
-  // have one slot per page of a sequence (the callers' buffers hold max_pages
-  // splits per row and head).
-  const bool balanced = a.R == 1 && a.B > 1 && a.B <= 64;
+  // Batches (up to 64 sequences): the balanced launch, where each (sequence,
+  // KV head) pair gets CTAs in proportion to its pages, so ragged contexts do
+  // not leave the longest sequences with the most rounds per CTA; one
+  // sequence: fixed splits of the page capacity. The partials of a balanced
+  // launch have one slot per page of a sequence (the callers' buffers hold
+  // max_pages splits per row and head).
+  const bool balanced = a.B > 1 && a.B <= 64;
   if (balanced) a.n_split = a.max_pages;
   size_t smem = attention_tc_smem(a.hd, QN, a.R);
   if (smem > 200 * 1024) return -2;
@@ -96,10 +94,8 @@ int attention_tc(const AttnArgs& a0, unsigned int* counters, int pps, cudaStream
   const size_t merge = ((size_t)QN * nsplit_max + 4) * 4 + (size_t)QN * nsplit_max * a.hd * 4;
   if (merge <= 200 * 1024) smem = std::max(smem, merge);
   cudaLaunchConfig_t cfg = {};
-  // balanced: one CTA per SM, or fewer when even full caches would give less
-  // than a round of page slots per CTA (CTAs without pages only wait and exit)
-  const long long cap_rounds = ((long long)a.B * a.nkv * a.max_pages + pw - 1) / pw;
-  const int nbal = (int)std::min<long long>(num_sms(), std::max<long long>(1, cap_rounds));
+  // balanced: one CTA per SM, and at least one per (sequence, KV head) pair
+  const int nbal = std::max(num_sms(), a.B * a.nkv);
   cfg.gridDim = balanced ? dim3(nbal) : dim3(a.B * a.nkv, a.n_split);
   cfg.blockDim = dim3(ATT_WARPS * 32);
   (void)qt;

@@ -221,15 +221,17 @@ struct AttnTc {
     run_split(a, bx, p0, p1, by, a.n_split, counters, smem, standalone, smem_bytes, pw_cap);
   }
 
-  // Balanced stand-alone launch: the pages of all (sequence, KV head) pairs,
-  // pair-major, are cut into equal contiguous ranges, one per CTA (at least a
-  // round of page slots each, so with few pages fewer CTAs work). A CTA's
-  // piece of a pair is one split of that pair; a pair's splits are numbered
-  // by CTA, so their partials and the merge order do not depend on timing.
+  // Balanced stand-alone launch for batches: each (sequence, KV head) pair
+  // gets one CTA plus a share of the remaining CTAs proportional to its pages
+  // (lengths read on the device, so the grid is fixed for graph capture),
+  // capped so that a CTA has at least a round of page slots; CTA j of a pair
+  // takes pages [np*j/k, np*(j+1)/k) as split j of k. Each CTA has one piece,
+  // and the longest sequences get the most CTAs.
   static SPEC_DEV void run_balanced(const AttnArgs& a, unsigned int* counters, unsigned char* smem,
                                     size_t smem_bytes) {
-    __shared__ int s_np[64];        // pages of each sequence
-    __shared__ long long s_off[65]; // first flattened page of each sequence
+    __shared__ int s_np[64];   // pages of each sequence
+    __shared__ int s_k[64];    // CTAs per pair of each sequence
+    __shared__ int s_kb[65];   // first CTA of each sequence's pairs
     const int nkv = a.nkv, B = a.B;
     const int G = a.nq / nkv, QT = (a.R * G + 15) / 16;
     const int PW = page_slots(QT, blockDim.x >> 5);
@@ -239,62 +241,43 @@ struct AttnTc {
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      long long acc = 0;
+      long long P = 0;
+      for (int b = 0; b < B; ++b) P += (long long)s_np[b] * nkv;
+      const long long extra = (long long)gridDim.x - (long long)B * nkv;  // CTAs beyond one per pair
+      int acc = 0;
       for (int b = 0; b < B; ++b) {
-        s_off[b] = acc;
-        acc += (long long)s_np[b] * nkv;
+        int k = 1;
+        if (extra > 0 && P > 0) k += (int)(((long long)s_np[b] * extra) / P);
+        k = min(k, max(1, s_np[b] / PW));
+        s_k[b] = k;
+        s_kb[b] = acc;
+        acc += k * nkv;
       }
-      s_off[B] = acc;
+      s_kb[B] = acc;
     }
     __syncthreads();
-    const long long P = s_off[B];
-    const long long want = (P + PW - 1) / PW;
-    const int ncta = (int)(want < (long long)gridDim.x ? want : (long long)gridDim.x);
     const int cta = blockIdx.x;
-    if (cta >= ncta) {
+    if (cta >= s_kb[B]) {
       grid_dep_wait();
       grid_dep_launch();
       return;
     }
-    auto begin = [&](int k) { return (P * k) / ncta; };
-    // CTA whose range holds flattened page q
-    auto owner = [&](long long q) {
-      int k = (int)(((q + 1) * ncta - 1) / P);
-      if (k >= ncta) k = ncta - 1;
-      while (k > 0 && begin(k) > q) --k;
-      while (k + 1 < ncta && begin(k + 1) <= q) ++k;
-      return k;
-    };
-    const long long q0 = begin(cta), q1 = begin(cta + 1);
-    // pages do not depend on the previous kernel: pull this CTA's K and V
+    int b = 0;
+    while (b + 1 < B && s_kb[b + 1] <= cta) ++b;
+    const int k = s_k[b], np = s_np[b];
+    const int kvh = (cta - s_kb[b]) / k, j = (cta - s_kb[b]) - kvh * k;
+    const int p0 = (int)(((long long)np * j) / k), p1 = (int)(((long long)np * (j + 1)) / k);
+    // pages do not depend on the previous kernel: pull this piece's K and V
     // planes towards L2 (one bulk prefetch per 16 KB plane) before the wait
     {
       const __nv_bfloat16* base = (const __nv_bfloat16*)a.pool + (size_t)a.layer * a.layer_elems;
-      for (long long i = q0 * 2 + threadIdx.x; i < q1 * 2; i += blockDim.x) {
-        const long long q = i >> 1;
-        int bb = 0;
-        while (bb + 1 < B && s_off[bb + 1] <= q) ++bb;
-        const int np = s_np[bb], kvh = (int)((q - s_off[bb]) / np);
-        const int p = (int)(q - s_off[bb] - (long long)kvh * np);
-        const int pg = a.block_table[(size_t)a.seq_ids[bb] * a.max_pages + p];
+      for (int i = threadIdx.x; i < (p1 - p0) * 2; i += blockDim.x) {
+        const int pg = a.block_table[(size_t)a.seq_ids[b] * a.max_pages + p0 + (i >> 1)];
         if (pg >= 0 && pg < a.n_pages)
-          prefetch_l2_bulk(base + (((size_t)pg * 2 + (int)(i & 1)) * nkv + kvh) * PAGE * HD, PAGE * HD * 2);
+          prefetch_l2_bulk(base + (((size_t)pg * 2 + (i & 1)) * nkv + kvh) * PAGE * HD, PAGE * HD * 2);
       }
     }
-    int b = 0;
-    for (long long q = q0; q < q1;) {
-      // sequence of flattened page q: the first b with s_off[b + 1] > q
-      while (b + 1 < B && s_off[b + 1] <= q) ++b;
-      const int np = s_np[b];
-      const int kvh = (int)((q - s_off[b]) / np);
-      const long long pair_first = s_off[b] + (long long)kvh * np;
-      const long long pair_end = pair_first + np;
-      const long long e = q1 < pair_end ? q1 : pair_end;
-      const int k0 = owner(pair_first), k1 = owner(pair_end - 1);
-      run_split(a, b * nkv + kvh, (int)(q - pair_first), (int)(e - pair_first), cta - k0, k1 - k0 + 1, counters,
-                smem, true, smem_bytes, 0);
-      q = e;
-    }
+    run_split(a, b * nkv + kvh, p0, p1, j, k, counters, smem, true, smem_bytes, 0);
   }
 
   // One split of (sequence, KV head) bx: pages [p0, p1) as split `split` of
