@@ -617,6 +617,16 @@ struct Cta {
     grid_dep_launch();
     if (e < 64) rms_s[e] = e < a.M ? __ldcg(inv_rms + e) : 0.f;
     if (p.map == MAP_ROPE) load_rope_tables();
+    if (a.epi == EPI_ADD) {
+      // the residual rows of this CTA's tiles towards L2 while the weights
+      // stream (the finish reads them; they may be out of L2 by now)
+      const int t0 = u0 / p.C, t1 = (u1 - 1) / p.C;
+      for (int i = e; i < (t1 - t0 + 1) * a.M; i += 128) {
+        const int t = t0 + i / a.M, m = i - (i / a.M) * a.M, n0 = t * TM;
+        const int cols = min(TM, a.N - n0);
+        if (cols > 0 && (cols & 3) == 0) prefetch_l2_bulk(a.Y + (size_t)m * a.ldy + n0, (unsigned)cols * 4);
+      }
+    }
     epi_sync();
     unsigned long long mybest = 0ull;
     SegIter it{u0, u1, p.C};
@@ -764,20 +774,23 @@ __global__ void __launch_bounds__(256) wide_prep_kernel(const float* X, int ldx,
                                                         float eps, int MP, uint16_t* xs, float* rms, int f16) {
   __shared__ float red[32];
   const int m = blockIdx.x;
+  // without a gain, blocks (m, y) split the row's columns (multiples of 8)
+  const int per = ((K + gridDim.y - 1) / gridDim.y + 7) / 8 * 8;
+  const int kb = blockIdx.y * per, ke = min(K, kb + per);
   grid_dep_wait();
   grid_dep_launch();
   uint16_t* hi = xs + (size_t)m * K;
   uint16_t* lo = xs + (size_t)(MP + m) * K;
   if (m >= M) {
-    for (int c8 = threadIdx.x * 8; c8 < K; c8 += blockDim.x * 8) {
+    for (int c8 = kb + threadIdx.x * 8; c8 < ke; c8 += blockDim.x * 8) {
       *reinterpret_cast<uint4*>(hi + c8) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(lo + c8) = make_uint4(0, 0, 0, 0);
     }
-    if (threadIdx.x == 0) rms[m] = 0.f;
+    if (threadIdx.x == 0 && blockIdx.y == 0) rms[m] = 0.f;
     return;
   }
   float ss = 0.f;
-  for (int c8 = threadIdx.x * 8; c8 < K; c8 += blockDim.x * 8) {
+  for (int c8 = kb + threadIdx.x * 8; c8 < ke; c8 += blockDim.x * 8) {
     const float4 u0 = __ldcg(reinterpret_cast<const float4*>(X + (size_t)m * ldx + c8));
     const float4 u1 = __ldcg(reinterpret_cast<const float4*>(X + (size_t)m * ldx + c8 + 4));
     float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
@@ -812,7 +825,7 @@ __global__ void __launch_bounds__(256) wide_prep_kernel(const float* X, int ldx,
   if (gain) {
     const float tot = block_sum(ss, red);
     if (threadIdx.x == 0) rms[m] = rsqrtf(tot / (float)K + eps);
-  } else if (threadIdx.x == 0) {
+  } else if (threadIdx.x == 0 && blockIdx.y == 0) {
     rms[m] = 1.f;
   }
 }
@@ -1004,7 +1017,9 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t pc = {};
-  pc.gridDim = dim3(p.MP);
+  // one block per row (the RMSNorm needs the whole row), else up to 2048
+  // columns per block
+  pc.gridDim = dim3(p.MP, a.gain ? 1 : (a.K + 2047) / 2048);
   pc.blockDim = dim3(256);
   pc.stream = st;
   pc.attrs = attr;
