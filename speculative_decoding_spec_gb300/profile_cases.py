@@ -9,6 +9,14 @@
         one layer of the E4B-shaped bf16 target (QKV, O, gate/up, down) and
         its LM head at M = 40 rows (batch 8, k = 4): the tcgen05 path, run
         twice. About 0.86 GB of weights, so nothing stays in L2.
+    python -m speculative_decoding_spec_gb300.profile_cases projections_wide_q4
+        one layer of the E2B-shaped Q4_0 target and its LM head at M = 20
+        rows (batch 4, k = 4): the tcgen05 path with shared-memory
+        dequantisation, run twice. About 0.24 GB of codes and scales.
+    python -m speculative_decoding_spec_gb300.profile_cases verify_q4b4
+        three verify passes of the E2B-shaped Q4_0 batch-4 workload (ctx
+        4096, k = 4; about 1.6 GB on the device): tcgen05 projections with
+        dequantisation, activation preparation and the balanced attention.
     python -m speculative_decoding_spec_gb300.profile_cases draft
         three draft calls (k = 3) on the E2B-shaped workload, one kernel per
         drafter operation (the default drafter).
@@ -70,6 +78,24 @@ def projections_wide(w):
         torch.cuda.synchronize()
 
 
+def projections_wide_q4(w):
+    t = configs.E2B_Q4
+    g = torch.Generator(device="cuda").manual_seed(4)
+    M = 20
+    seq = [(synth.make_matrix(g, t.wdtype, 1, N, K, t.wstd, "cuda"), K)
+           for N, K in ((t.nqkv, t.d), (t.d, t.nq * t.hd), (2 * t.ff, t.d), (t.d, t.ff), (t.V, t.d))]
+    xs = {K: torch.randn((M, K), device="cuda") for _, K in seq}
+    ys = [torch.empty((M, W.N), device="cuda") for W, _ in seq]
+    for _ in range(2):
+        for (W, K), y in zip(seq, ys):
+            binding.spec_linear(W, xs[K], y=y)
+        torch.cuda.synchronize()
+
+
+def verify_q4b4(w):
+    verify(configs.WORKLOADS["e2b_q4_0_b4_ctx4096_k4"])
+
+
 def draft(w, cluster=False):
     _, eng, ids = _engine(w)
     eng.set_option(binding.SPEC_OPT_DRAFT_CLUSTER, int(cluster))
@@ -84,13 +110,14 @@ def draft_cluster(w):
 
 def verify(w):
     _, eng, ids = _engine(w)
-    d = eng._in("d", torch.tensor([[1, 2, 3]], dtype=torch.int32))
+    d = eng._in("d", torch.arange(1, 1 + w.B * w.k, dtype=torch.int32).view(w.B, w.k))
     for _ in range(3):
         eng.spec_verify(ids, d)
     eng.sync()
 
 
-CASES = {"projections": projections, "projections_wide": projections_wide, "draft": draft, "draft_cluster": draft_cluster, "verify": verify}
+CASES = {"projections": projections, "projections_wide": projections_wide,
+         "projections_wide_q4": projections_wide_q4, "verify_q4b4": verify_q4b4, "draft": draft, "draft_cluster": draft_cluster, "verify": verify}
 
 
 def main(argv):
