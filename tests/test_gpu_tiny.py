@@ -51,6 +51,28 @@ def _prefilled(models, graphs=True, persistent=False, draft_cluster=False):
     return eng, ids
 
 
+def test_prefill_two_sequences_matches_oracle(models):
+    """Two 64-token prompts in one prefill: 128 rows, which the bf16 / Q4_0
+    projections run as two 64-row passes (the tail after the second)."""
+    tw, dw, T, D, prompt, s0 = models
+    eng = _engine(tw, dw)
+    ids = eng.seq_ids([0, 1])
+    second = synth.make_tokens(64, W.target.V, seed=synth.SEED_KV + 7)
+    both = torch.stack([second, prompt]).cuda()
+    eng.spec_prefill(ids, eng._in("prompts", both))
+    eng.sync()
+    s1 = oracle.Seq(T, CAP)
+    m1 = oracle.prefill(T, s1, second.numpy())
+    tol = TOL[tw.shape.wdtype]
+    for slot, ref in ((0, s1), (1, s0)):
+        assert int(eng.seq_len[slot]) == 64
+        assert_rows_close(eng.hid[slot:slot + 1].cpu().numpy(), ref.hid[None], tol, "prefill hidden %d" % slot)
+    assert int(eng.pending[1]) == s0.pending
+    if m1 > MARGIN:
+        assert int(eng.pending[0]) == s1.pending
+    eng.close()
+
+
 def test_prefill_matches_oracle(models):
     tw, dw, T, D, prompt, s0 = models
     eng, ids = _prefilled(models)
