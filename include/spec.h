@@ -293,8 +293,11 @@ spec_status spec_set_graphs(spec_ctx *ctx, int32_t enable);
 #define SPEC_OPT_DRAFT_TRACE 6
 /*  SPEC_OPT_WIDE_TRACE  value = a device pointer to a zeroed uint64 buffer of at
  *                       least 256 * n_SMs * 16 entries, or 0: the next 256
- *                       enqueued launches of the tcgen05 projection (passes of
- *                       more than 8 rows) record, per CTA, globaltimer stamps
+ *                       enqueued projections record per-CTA globaltimer stamps.
+ *                       A register-fragment launch (at most 8 rows, bf16 or
+ *                       Q4_0) uses slots 2 entry, 3 past the launch dependency,
+ *                       0 activations staged, 1 main loop done, 4 done. A
+ *                       tcgen05 launch (passes of more than 8 rows) records
  *                       (ns) in 16 slots: 0 entry, 1 setup done, 2 producer past
  *                       the launch dependency, 3 first stage consumed, 4 last
  *                       MMA issued, 5 last accumulator ready, 6 epilogue done,

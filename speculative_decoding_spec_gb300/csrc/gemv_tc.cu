@@ -12,6 +12,7 @@ __global__ void __launch_bounds__(TW_DEFAULT * 32, 1) gemv_tc_kernel(GemvArgs a,
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Sk<TW_DEFAULT, Q4> k{a, p, map};
   sk_bind(k, smem_raw, fix, cnt, blockIdx.x, true);
+  k.trace = a.tc_trace ? a.tc_trace + (size_t)blockIdx.x * 16 : nullptr;
   k.run();
 }
 

@@ -143,7 +143,8 @@ struct Sk {
   unsigned int* cnt;        // global [T]
   int bid;                  // this CTA's index in the launch (or phase)
   bool standalone;          // own launch (PDL waits) or a phase of the persistent pass kernel
-  unsigned long long* trace;  // optional: [0] after staging, [1] after the main loop
+  unsigned long long* trace;  // optional: [0] after staging, [1] after the main loop; stand-alone
+                              // launches also [2] entry, [3] past the dependency wait, [4] done
 
   // MAP_ROPE: tile t covers elements 8u..8u+7 of head h (row g) and the
   // elements hd/2 further on (row g+8), the pairs RoPE rotates together
@@ -453,10 +454,12 @@ struct Sk {
     // towards L2 (capped) and put the first unit in flight before the wait
     uint4 wa[4], wb[4];
     if (standalone) {
+      if (trace && threadIdx.x == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(trace[2]));
       if (a.prefetch && !Q4) prefetch_slice(u0, u1);
       if (wa_ < wb_) load_unit(wa_, wa, wb);
       grid_dep_wait();
       grid_dep_launch();
+      if (trace && threadIdx.x == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(trace[3]));
     }
     if (threadIdx.x < TW * 2) seg_tag[threadIdx.x] = -1;
     stage();
@@ -548,6 +551,7 @@ struct Sk {
       }
     }
     if (a.epi == EPI_ARGMAX) argmax_tail(mybest);
+    if (standalone && trace && threadIdx.x == 0) asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(trace[4]));
   }
 
   // CTA whose unit range holds unit u

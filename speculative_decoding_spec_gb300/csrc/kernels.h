@@ -99,6 +99,7 @@ struct GemvArgs {
   int pdl;                  // launch with programmatic dependent launch
   int prefetch;             // tensor-core kernel: pull the CTA's weight slice to L2 first
   WideScratch wide;         // tcgen05 path for more than 8 rows (bf16 weights)
+  unsigned long long* tc_trace;  // optional [grid][16] globaltimer stamps of a register-fragment launch
 };
 int gemv(const GemvArgs& a, cudaStream_t st);
 

@@ -457,8 +457,11 @@ int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st) {
   g.tc_fix = c->wk.tc_fix;
   g.tc_cnt = c->wk.tc_cnt;
   g.wide = c->wk.wide;
-  if (c->wtrace && c->wtrace_n < WTRACE_LAUNCHES && g.M > 8)
-    g.wide.trace = c->wtrace + (size_t)(c->wtrace_n++) * num_sms() * 16;
+  if (c->wtrace && c->wtrace_n < WTRACE_LAUNCHES) {
+    unsigned long long* slot = c->wtrace + (size_t)(c->wtrace_n++) * num_sms() * 16;
+    if (g.M > 8) g.wide.trace = slot;
+    else g.tc_trace = slot;
+  }
   g.prefetch = c->prefetch ? 1 : 0;
   return gemv(g, st);
 }
