@@ -9,7 +9,7 @@
 // to keep up with HBM, while a 128-row weight tile times a 16-64-row activation
 // tile is a natural tcgen05 shape (M = 128 weight rows, N = rows padded to 16).
 //
-// Data flow per CTA (one CTA of 6 warps per SM):
+// Data flow per CTA (one CTA per SM: 6 warps, 10 with Q4_0 weights):
 //  - warp 0 (one thread): TMA producer. A ring of stages, each one 128 x 64
 //    bf16 weight tile and the matching 64 columns of the activation hi and lo
 //    planes, both in the 128-byte-swizzled K-major layout the MMA reads.
@@ -40,7 +40,11 @@
 // Work split: units are (tile, 64-column chunk) pairs in tile-major order and
 // CTA b owns the balanced range [U*b/G, U*(b+1)/G). A tile cut between CTAs is
 // summed by the last CTA to arrive (arrival counter per tile), in CTA order, so
-// results do not depend on timing.
+// results do not depend on timing. Matrices with few tiles run instead as one
+// thread-block cluster of S CTAs per tile: each CTA streams a K-range and keeps
+// its partial in shared memory; after a cluster barrier each CTA sums a slice
+// of the activation rows over the cluster's CTAs in rank order (distributed
+// shared memory) and finishes those rows.
 //
 // Every wait is bounded: on a timeout the CTA records SPEC_ERR_TIMEOUT, stops,
 // drains its own copies and MMAs, frees its tensor memory and returns.
