@@ -120,13 +120,42 @@ __global__ void __launch_bounds__(256) members_kernel(ClusterArgs a) {
   const int cl = a.chosen[b * a.top_c + ci];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned long long best = 0ull;
-  for (int r = warp; r < a.cs; r += 8) {
-    const long long p = (long long)cl * a.cs + r;
-    float acc = 0.f;
-    for (int c = lane; c < h; c += 32) acc = fmaf(ub[c], elem(a.vocab, h, p, c), acc);
-    acc = warp_sum(acc);
-    const unsigned long long key = pack_best(acc, (uint32_t)a.perm[p]);
-    best = key > best ? key : best;
+  if (a.vocab.dtype == DT_BF16 && h == 256 && a.cs % 64 == 0) {
+    // bf16 rows of 256: lane i holds elements 8i..8i+7 of the state and
+    // loads its 16 bytes of each of the warp's rows, 8 rows in flight at a time
+    float uv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) uv[i] = ub[8 * lane + i];
+    const __nv_bfloat16* V = (const __nv_bfloat16*)a.vocab.data;
+    for (int r0 = warp; r0 < a.cs; r0 += 64) {
+      uint4 q[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        q[j] = ldg_stream(V + ((long long)cl * a.cs + r0 + 8 * j) * 256 + 8 * lane);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t wv[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc = fmaf(uv[2 * i], bf16lo(wv[i]), acc);
+          acc = fmaf(uv[2 * i + 1], bf16hi(wv[i]), acc);
+        }
+        acc = warp_sum(acc);
+        const long long p = (long long)cl * a.cs + r0 + 8 * j;
+        const unsigned long long key = pack_best(acc, (uint32_t)a.perm[p]);
+        best = key > best ? key : best;
+      }
+    }
+  } else {
+    for (int r = warp; r < a.cs; r += 8) {
+      const long long p = (long long)cl * a.cs + r;
+      float acc = 0.f;
+      for (int c = lane; c < h; c += 32) acc = fmaf(ub[c], elem(a.vocab, h, p, c), acc);
+      acc = warp_sum(acc);
+      const unsigned long long key = pack_best(acc, (uint32_t)a.perm[p]);
+      best = key > best ? key : best;
+    }
   }
   if (lane == 0) wbest[warp] = best;
   __syncthreads();
