@@ -38,6 +38,9 @@ def lib():
         _lib.or_argmax_f32.restype = i
         _lib.or_argmax_f32.argtypes = [p, i, p]
         _lib.or_forward.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), p, i, p, p, p, p]
+        _lib.or_forward_resid.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), p, i, p, p, p, p, p]
+        _lib.or_draft_states.argtypes = [C.POINTER(OrModel), C.POINTER(OrDrafter), C.POINTER(OrSeq),
+                                         i, p, p, p, p]
         _lib.or_prefill.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), p, i, p]
         _lib.or_accept.restype = i
         _lib.or_accept.argtypes = [i, p, p]
@@ -199,6 +202,22 @@ def forward(t: Target, s: Seq, tokens, want_logits=False):
     return am, mg, hid, lg
 
 
+def forward_resid(t: Target, s: Seq, tokens):
+    """forward() plus the residual stream after the last layer (before the
+    final RMSNorm). Returns (argmax, margin, hidden, logits, resid[R][d])."""
+    tok = _i32(tokens)
+    R = tok.shape[0]
+    am = np.zeros(R, np.int32)
+    mg = np.zeros(R, np.float64)
+    hid = np.zeros((R, t.shape.d), np.float64)
+    lg = np.zeros((R, t.shape.V), np.float64)
+    res = np.zeros((R, t.shape.d), np.float64)
+    rc = lib().or_forward_resid(C.byref(t.m), C.byref(s.c), _ptr(tok), R, _ptr(lg), _ptr(am),
+                                _ptr(mg), _ptr(hid), _ptr(res))
+    assert rc == 0, "or_forward_resid failed (capacity?)"
+    return am, mg, hid, lg, res
+
+
 def prefill(t: Target, s: Seq, tokens) -> float:
     tok = _i32(tokens)
     mg = C.c_double()
@@ -239,6 +258,18 @@ def draft(t: Target, dr: Drafter, s: Seq, k: int):
     rc = lib().or_draft(C.byref(t.m), C.byref(dr.m), C.byref(s.c), k, _ptr(out), _ptr(mg))
     assert rc == 0
     return out, mg
+
+
+def draft_states(t: Target, dr: Drafter, s: Seq, k: int):
+    """draft() plus per-step states: (drafts, margins, u_bar[k][h], h_next[k][bh])."""
+    out = np.zeros(k, np.int32)
+    mg = np.zeros(k, np.float64)
+    ub = np.zeros((k, dr.shape.h), np.float64)
+    hn = np.zeros((k, dr.shape.bh), np.float64)
+    rc = lib().or_draft_states(C.byref(t.m), C.byref(dr.m), C.byref(s.c), k, _ptr(out), _ptr(mg),
+                               _ptr(ub), _ptr(hn))
+    assert rc == 0
+    return out, mg, ub, hn
 
 
 def draft_head(dr: Drafter, u_bar) -> tuple:

@@ -234,6 +234,15 @@ static float *kv_at(const or_model *m, const or_seq *s, int l, int which, int h)
 int or_forward(const or_model *m, or_seq *s, const int32_t *tokens, int R,
                double *logits, int32_t *argmax, double *margin, double *hid)
 {
+    return or_forward_resid(m, s, tokens, R, logits, argmax, margin, hid, NULL);
+}
+
+/* or_forward that also hands out the residual stream x of every row after the
+ * last layer, before the final RMSNorm (resid [R][d], optional). */
+int or_forward_resid(const or_model *m, or_seq *s, const int32_t *tokens, int R,
+                     double *logits, int32_t *argmax, double *margin, double *hid,
+                     double *resid)
+{
     if (R <= 0 || s->len + R > s->cap)
         return -1;
     const int d = m->d, hd = m->hd, qd = m->nq * hd, kd = m->nkv * hd;
@@ -297,6 +306,8 @@ int or_forward(const or_model *m, or_seq *s, const int32_t *tokens, int R,
             x[i] += tmp[i];
     }
 
+    if (resid)
+        memcpy(resid, x, sizeof(double) * (size_t)R * d);
     for (int r = 0; r < R; ++r)
         or_rmsnorm(x + (int64_t)r * d, d, m->g_final, m->eps, xn + (int64_t)r * d);
     if (hid)
@@ -481,6 +492,15 @@ int or_draft_head(const or_drafter *dr, const double *u_bar, double *margin)
 int or_draft(const or_model *m, const or_drafter *dr, const or_seq *s, int k,
              int32_t *drafts, double *margins)
 {
+    return or_draft_states(m, dr, s, k, drafts, margins, NULL, NULL);
+}
+
+/* or_draft that also hands out, per step j, the normalised drafter state the
+ * head reads (u_bar [k][h]) and the next hidden state h_j (h_next [k][bh]);
+ * both optional. */
+int or_draft_states(const or_model *m, const or_drafter *dr, const or_seq *s, int k,
+                    int32_t *drafts, double *margins, double *u_bar, double *h_next)
+{
     const int h = dr->h, bh = dr->bh, hd = dr->hd, qd = dr->nq * hd, ff = dr->ff;
     const int grp = dr->nq / dr->nkv;
     if (bh != m->d || hd != m->hd || dr->nkv != m->nkv)
@@ -530,6 +550,10 @@ int or_draft(const or_model *m, const or_drafter *dr, const or_seq *s, int k,
         }
         or_linear(&dr->w_out, bh, h, u, 1, hprev);
         or_rmsnorm(u, h, dr->g_out, m->eps, un);
+        if (u_bar)
+            memcpy(u_bar + (int64_t)(j - 1) * h, un, sizeof(double) * h);
+        if (h_next)
+            memcpy(h_next + (int64_t)(j - 1) * bh, hprev, sizeof(double) * bh);
         tok = or_draft_head(dr, un, margins ? margins + (j - 1) : NULL);
         drafts[j - 1] = tok;
     }

@@ -111,6 +111,11 @@ int    or_argmax_f32(const double *logits, int n, double *margin);
  * the rows' K/V into the cache (len is NOT advanced). Outputs are optional. */
 int or_forward(const or_model *m, or_seq *s, const int32_t *tokens, int R,
                double *logits, int32_t *argmax, double *margin, double *hid);
+/* or_forward plus the residual stream of every row after the last layer,
+ * before the final RMSNorm (resid [R][d], optional). */
+int or_forward_resid(const or_model *m, or_seq *s, const int32_t *tokens, int R,
+                     double *logits, int32_t *argmax, double *margin, double *hid,
+                     double *resid);
 /* Prompt processing: forward, commit all R rows, pending = argmax of the last
  * row, hid = its hidden. */
 int or_prefill(const or_model *m, or_seq *s, const int32_t *tokens, int R,
@@ -127,6 +132,10 @@ int or_greedy(const or_model *m, or_seq *s, int n, int32_t *out, double *margins
 /* ---- drafter ---- */
 int or_draft(const or_model *m, const or_drafter *dr, const or_seq *s, int k,
              int32_t *drafts, double *margins);
+/* or_draft plus, per step j, the normalised state the head reads
+ * (u_bar [k][h]) and the next hidden state h_j = W_out . u (h_next [k][bh]). */
+int or_draft_states(const or_model *m, const or_drafter *dr, const or_seq *s, int k,
+                    int32_t *drafts, double *margins, double *u_bar, double *h_next);
 /* The drafter's output head on one normalised drafter state u_bar [h]. */
 int or_draft_head(const or_drafter *dr, const double *u_bar, double *margin);
 

@@ -8,7 +8,8 @@ available, so these stand in for the pages' coding / summarisation prompts):
 * linear weights, embedding (tied LM head) and drafter tables: N(0, wstd),
   wstd = 0.02 (0.01 for the ~30B model), stored in the model's weight dtype;
   Q4_0 weights: codes uniform on 0..15, fp16 scales |N(0, 0.004)|;
-* norm gains: 1;
+* norm gains: 1 + N(0, 0.1) per element, from their own seeded stream (so that
+  a gain read from the wrong layer or the wrong norm changes the result);
 * the drafter's clustered vocabulary: a random permutation of the token ids
   sorted into 2048 balanced clusters; for float tables each member row is its
   centroid row plus N(0, wstd/2) noise, so the top clusters hold the best rows;
@@ -16,7 +17,7 @@ available, so these stand in for the pages' coding / summarisation prompts):
 * pre-filled KV for long contexts: N(0, 1) in the cache dtype (keys taken as
   already rotated);
 * page tables: a seeded shuffle of the page pool.
-Seeds: weights 0, KV 1, tokens 2, acceptance draws 3.
+Seeds: weights 0, KV 1, tokens 2, acceptance draws 3; gains: the weight seed + 1000.
 """
 from dataclasses import dataclass
 from typing import Dict, List, Optional
@@ -26,6 +27,8 @@ import torch
 from .configs import BF16, F32, PAGE, Q4_0, DrafterShape, TargetShape
 
 SEED_WEIGHTS, SEED_KV, SEED_TOKENS, SEED_ALPHA = 0, 1, 2, 3
+SEED_GAINS = 1000       # offset of the norm-gain stream from the weight seed
+GAIN_STD = 0.1
 
 
 @dataclass
@@ -63,6 +66,16 @@ def _normal(g, shape, std, dtype, device, chunk_rows=4096) -> torch.Tensor:
         r1 = min(flat.shape[0], r0 + chunk_rows)
         flat[r0:r1] = (torch.randn((r1 - r0, shape[-1]), generator=g, device=device) * std).to(dtype)
     return out
+
+
+def _gains(seed: int, device):
+    """Draws RMSNorm gain vectors 1 + N(0, GAIN_STD) (float32) one after another
+    from one seeded stream."""
+    g = _gen(seed, device)
+
+    def draw(*shape):
+        return 1.0 + torch.randn(shape, generator=g, device=device) * GAIN_STD
+    return draw
 
 
 def _q4_0(g, L, N, K, device, chunk_rows=4096) -> WTensor:
@@ -110,9 +123,9 @@ def make_target(t: TargetShape, device="cpu", seed=SEED_WEIGHTS) -> TargetWeight
     wo = w(t.L, t.d, t.nq * t.hd)
     wgu = w(t.L, 2 * t.ff, t.d)
     wdown = w(t.L, t.d, t.ff)
-    ones = lambda *s: torch.ones(s, dtype=torch.float32, device=device)
-    return TargetWeights(t, embed, wqkv, wo, wgu, wdown, ones(t.L, t.d), ones(t.L, t.d),
-                         ones(t.d))
+    gains = _gains(seed + SEED_GAINS, device)
+    return TargetWeights(t, embed, wqkv, wo, wgu, wdown, gains(t.L, t.d), gains(t.L, t.d),
+                         gains(t.d))
 
 
 @dataclass
@@ -163,9 +176,9 @@ def make_drafter(dsh: DrafterShape, device="cpu", seed=SEED_WEIGHTS + 100) -> Dr
             vocab = WTensor(dsh.wdtype, 1, dsh.V, dsh.h, members.to(tdt))
     else:
         vocab = w(1, dsh.V, dsh.h)
-    ones = lambda *s: torch.ones(s, dtype=torch.float32, device=device)
-    return DrafterWeights(dsh, w_in, ones(dsh.bh), ones(dsh.bh), wq, wo, wgu, wdown,
-                          ones(dsh.L, dsh.h), ones(dsh.L, dsh.h), ones(dsh.h), w_out, vocab,
+    gains = _gains(seed + SEED_GAINS, device)
+    return DrafterWeights(dsh, w_in, gains(dsh.bh), gains(dsh.bh), wq, wo, wgu, wdown,
+                          gains(dsh.L, dsh.h), gains(dsh.L, dsh.h), gains(dsh.h), w_out, vocab,
                           centroids, perm)
 
 
