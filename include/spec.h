@@ -232,7 +232,10 @@ spec_status spec_linear(const spec_matrix *w, int32_t N, int32_t K, const float 
  * no counterpart of this call: it only moves spec_linear's scratch (split-tile
  * partials and arrival counters) into a fixed 512 KiB array in the library's
  * device image, held by every GPU that loads the library until the process
- * exits. Same arguments and results as spec_linear otherwise.
+ * exits. Same arguments and results as spec_linear otherwise, with one
+ * difference in how the work runs: M > 8 rows run as passes of 8 rows on the
+ * register-fragment kernel, each pass streaming W again (spec_linear runs 9-64
+ * rows in one tcgen05 pass, whose activation planes would not fit the array).
  *  - N may be at most SPEC_LINEAR_NOALLOC_MAX_ROWS; larger N returns
  *    SPEC_ECAPACITY without launching anything.
  *  - The first call on a device looks up the array's address with that device
@@ -245,6 +248,36 @@ spec_status spec_linear(const spec_matrix *w, int32_t N, int32_t K, const float 
 spec_status spec_linear_noalloc(const spec_matrix *w, int32_t N, int32_t K, const float *x, int32_t M,
                                 const float *gain, float eps, float *y, void *stream);
 
+/* One attention launch over the paged cache, the kernels every pass runs (a
+ * kernel-level entry for checks and timing; the passes call the same code).
+ * Causal attention of the verified rows ("Gemma 4's MTP drafter explained"
+ * (molayo1419.me), section "How does speculative decoding work?": the target
+ * checks every drafted position in one pass): with key_extra = 1, row i of
+ * sequence b sits at position seq_len[seq_ids[b]] + i, its key and value are
+ * already in the cache, and it attends keys [0, seq_len + i]; with key_extra =
+ * 0 every row of sequence b attends [0, seq_len) (the drafter's
+ * cross-attention into the target's cache, "Accelerating Gemini Nano on Pixel
+ * with frozen multi-token prediction" (ai-news-spoon), "Zero-copy
+ * architecture"). Scores are q.k / sqrt(head_dim), softmax in fp32.
+ *  m: head_dim, n_kv_heads, kv_dtype and n_layers describe the cache (other
+ *     fields must be valid but are unused); kv: the cache; layer: which layer.
+ *  seq_ids ("device" int32 [B]) and seq_len ("device" int32 [n_slots]).
+ *  q ("device" float [B*R][n_q_heads*head_dim], row b*R+i, head h at column
+ *     h*head_dim, already rotated); query head h reads KV head
+ *     h / (n_q_heads / n_kv_heads). out ("device" float, same shape).
+ *  workspace ("device", ws_bytes >= spec_attention_workspace_bytes(m, B, R,
+ *     n_q_heads, kv->max_pages_per_seq)): zeroed before its first use; the
+ *     kernels leave it zeroed except the split partials.
+ * B <= 64, R <= 64, R * n_q_heads / n_kv_heads <= 128. A page id out of range
+ * is skipped and recorded in the workspace's first int (SPEC_ECAPACITY's
+ * device code 2). Asynchronous on `stream`. */
+size_t spec_attention_workspace_bytes(const spec_model_desc *m, int32_t B, int32_t R, int32_t n_q_heads,
+                                      int32_t max_pages_per_seq);
+spec_status spec_attention(const spec_model_desc *m, const spec_kv_desc *kv, int32_t layer, int32_t B,
+                           const int32_t *seq_ids, const int32_t *seq_len, int32_t R, int32_t n_q_heads,
+                           int32_t key_extra, const float *q, float *out, void *workspace, size_t ws_bytes,
+                           void *stream);
+
 /* Copy one slot's counters to the host (synchronises `stream`). */
 spec_status spec_stats(spec_ctx *ctx, int32_t slot, spec_stats_t *out, void *stream);
 
@@ -255,42 +288,22 @@ spec_status spec_sync(spec_ctx *ctx, void *stream);
  * for non-NULL streams). */
 spec_status spec_set_graphs(spec_ctx *ctx, int32_t enable);
 
-/* Execution options (for comparisons):
+/* Execution options:
  *  SPEC_OPT_GRAPHS      (default 1) capture each call shape in a CUDA graph
  *                       and replay it;
- *  SPEC_OPT_PERSISTENT  (default 0) run a bf16 target pass of at most 8 rows
- *                       as one persistent kernel (all SMs walk the pass's steps
- *                       with a bounded grid barrier between them) instead of
- *                       one kernel per step;
- *  SPEC_OPT_TRACE       value = a device pointer to a uint64 buffer of at least
- *                       (3 + 5*n_layers) * n_SMs * 6 entries, or 0: the
- *                       persistent pass records, per step and CTA, the step's
- *                       start, two marks inside a projection step (activations
- *                       staged, main loop done), the end of the step's work
- *                       and the arrival at the barrier after it (globaltimer,
- *                       ns; slot 5 unused).
+ *  SPEC_OPT_PREFETCH    (default 0) each projection CTA first pulls its share
+ *                       of the weights towards L2 (bulk L2 prefetch).
  * Changing an option drops the captured graphs. */
 #define SPEC_OPT_GRAPHS 1
-#define SPEC_OPT_PERSISTENT 2
-#define SPEC_OPT_TRACE 3
-/*  SPEC_OPT_PREFETCH    (default 0) each projection CTA first pulls its share
- *                       of the weights towards L2 (bulk L2 prefetch); in the
- *                       persistent pass, of the next step's weights or KV
- *                       pages before the grid barrier. */
 #define SPEC_OPT_PREFETCH 4
-/*  SPEC_OPT_DRAFT_CLUSTER (default 0) run all k drafter steps as one launch of
- *                       one thread-block cluster per sequence (weights
- *                       streamed through shared memory by bulk copies,
- *                       activations exchanged through distributed shared
- *                       memory); 0, or shapes it does not cover, run one
- *                       kernel per drafter operation over the whole GPU. */
-#define SPEC_OPT_DRAFT_CLUSTER 5
-/*  SPEC_OPT_DRAFT_TRACE value = a device pointer to a uint64 buffer of at least
- *                       1 + k * (7 + 10 * n_drafter_layers) entries, or 0: the
- *                       fused drafter records, for sequence 0, globaltimer
- *                       stamps (ns) at its start, after each operation's last
- *                       weight chunk and after each cluster barrier. */
-#define SPEC_OPT_DRAFT_TRACE 6
+/*  SPEC_OPT_TEST_ATTN_WAIT (default 0; for failure-detection tests only) 1:
+ *                       the split merge of the tensor-core attention waits for
+ *                       one more arrival than there are splits, so its bounded
+ *                       wait (about one second) runs out: the launch records
+ *                       a timeout, skips the merge and returns, and the pass
+ *                       commits nothing; spec_sync then reports SPEC_ETIMEOUT
+ *                       and later passes run normally once the option is 0. */
+#define SPEC_OPT_TEST_ATTN_WAIT 8
 /*  SPEC_OPT_WIDE_TRACE  value = a device pointer to a zeroed uint64 buffer of at
  *                       least 256 * n_SMs * 16 entries, or 0: the next 256
  *                       enqueued projections record per-CTA globaltimer stamps.

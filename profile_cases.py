@@ -1,38 +1,46 @@
 """Small, self-contained GPU cases for profiling the hot kernels with ncu.
+Each summary under profiles/ names the case and the ncu command it ran.
 
-    python -m speculative_decoding_spec_gb300.profile_cases projections
+    python profile_cases.py projections
         every projection of one verify pass of the E2B-shaped bf16 target
         (24 layers x QKV, O, gate/up, down, then the LM head; M = 4 rows),
-        run twice -- the launch sequence whose average the bench's roofline
-        line reports. About 2.5 GB of weights, so nothing stays in L2.
-    python -m speculative_decoding_spec_gb300.profile_cases projections_wide
+        run twice. About 2.5 GB of weights, so nothing stays in L2.
+    python profile_cases.py projections_wide
         one layer of the E4B-shaped bf16 target (QKV, O, gate/up, down) and
         its LM head at M = 40 rows (batch 8, k = 4): the tcgen05 path, run
-        twice. About 0.86 GB of weights, so nothing stays in L2.
-    python -m speculative_decoding_spec_gb300.profile_cases projections_wide_q4
+        twice. About 0.86 GB of weights.
+    python profile_cases.py projections_30b
+        one layer of the ~30B-class bf16 target (QKV, O, gate/up, down: 1.08
+        GB) and its LM head (3.2 GB) at M = 40 rows (batch 8, k = 4), run
+        twice: the matrix shapes of the bench's roofline kernel.
+    python profile_cases.py projections_30b_m5
+        the same shapes at M = 5 rows (batch 1, k = 4).
+    python profile_cases.py projections_wide_q4
         one layer of the E2B-shaped Q4_0 target and its LM head at M = 20
         rows (batch 4, k = 4): the tcgen05 path with shared-memory
         dequantisation, run twice. About 0.24 GB of codes and scales.
-    python -m speculative_decoding_spec_gb300.profile_cases verify_q4b4
+    python profile_cases.py verify_q4b4
         three verify passes of the E2B-shaped Q4_0 batch-4 workload (ctx
-        4096, k = 4; about 1.6 GB on the device): tcgen05 projections with
-        dequantisation, activation preparation and the balanced attention.
-    python -m speculative_decoding_spec_gb300.profile_cases draft
-        three draft calls (k = 3) on the E2B-shaped workload, one kernel per
-        drafter operation (the default drafter).
-    python -m speculative_decoding_spec_gb300.profile_cases draft_cluster
-        the same with the one-cluster fused drafter.
-    python -m speculative_decoding_spec_gb300.profile_cases verify
+        4096, k = 4; about 1.6 GB on the device).
+    python profile_cases.py draft
+        three draft calls (k = 3) on the E2B-shaped workload.
+    python profile_cases.py verify
         three verify passes (k = 3) of the E2B-shaped workload.
+    python profile_cases.py attention_30b
+        the verify attention of the ~30B-class model at batch 8, context
+        8192, k = 4 (one layer's cache: 268 MB), three launches.
 
-Inputs are the seeded synthetic weights and caches of the workload; nothing
+Inputs are the seeded synthetic weights and caches of the workloads; nothing
 here checks results (the tests do).
 """
+import os
 import sys
 
 import torch
 
-from . import binding, configs, synth
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+from speculative_decoding_spec_gb300 import binding, configs, synth  # noqa: E402
 
 WORKLOAD = "e2b_bf16_b1_ctx2048_k3"
 
@@ -64,10 +72,8 @@ def projections(w):
         torch.cuda.synchronize()
 
 
-def projections_wide(w):
-    t = configs.E4B
-    g = torch.Generator(device="cuda").manual_seed(3)
-    M = 40
+def _one_layer_and_head(t, M, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
     seq = [(synth.make_matrix(g, t.wdtype, 1, N, K, t.wstd, "cuda"), K)
            for N, K in ((t.nqkv, t.d), (t.d, t.nq * t.hd), (2 * t.ff, t.d), (t.d, t.ff), (t.V, t.d))]
     xs = {K: torch.randn((M, K), device="cuda") for _, K in seq}
@@ -76,36 +82,33 @@ def projections_wide(w):
         for (W, K), y in zip(seq, ys):
             binding.spec_linear(W, xs[K], y=y)
         torch.cuda.synchronize()
+
+
+def projections_wide(w):
+    _one_layer_and_head(configs.E4B, 40, 3)
+
+
+def projections_30b(w):
+    _one_layer_and_head(configs.DENSE30B, 40, 5)
+
+
+def projections_30b_m5(w):
+    _one_layer_and_head(configs.DENSE30B, 5, 5)
 
 
 def projections_wide_q4(w):
-    t = configs.E2B_Q4
-    g = torch.Generator(device="cuda").manual_seed(4)
-    M = 20
-    seq = [(synth.make_matrix(g, t.wdtype, 1, N, K, t.wstd, "cuda"), K)
-           for N, K in ((t.nqkv, t.d), (t.d, t.nq * t.hd), (2 * t.ff, t.d), (t.d, t.ff), (t.V, t.d))]
-    xs = {K: torch.randn((M, K), device="cuda") for _, K in seq}
-    ys = [torch.empty((M, W.N), device="cuda") for W, _ in seq]
-    for _ in range(2):
-        for (W, K), y in zip(seq, ys):
-            binding.spec_linear(W, xs[K], y=y)
-        torch.cuda.synchronize()
+    _one_layer_and_head(configs.E2B_Q4, 20, 4)
 
 
 def verify_q4b4(w):
     verify(configs.WORKLOADS["e2b_q4_0_b4_ctx4096_k4"])
 
 
-def draft(w, cluster=False):
+def draft(w):
     _, eng, ids = _engine(w)
-    eng.set_option(binding.SPEC_OPT_DRAFT_CLUSTER, int(cluster))
     for _ in range(3):
         eng.spec_draft(ids, w.B, w.k)
     eng.sync()
-
-
-def draft_cluster(w):
-    draft(w, cluster=True)
 
 
 def verify(w):
@@ -116,14 +119,33 @@ def verify(w):
     eng.sync()
 
 
-CASES = {"projections": projections, "projections_wide": projections_wide,
-         "projections_wide_q4": projections_wide_q4, "verify_q4b4": verify_q4b4, "draft": draft, "draft_cluster": draft_cluster, "verify": verify}
+def attention_30b(w):
+    t = configs.DENSE30B
+    B, R, ctx = 8, 5, 8192
+    shape = configs.TargetShape(**{**t.__dict__, "L": 1})
+    pages = (ctx + 63) // 64
+    g = torch.Generator(device="cuda").manual_seed(9)
+    pool = torch.randn((1, B * pages, 2, t.nkv, 64, t.hd), generator=g, device="cuda").to(torch.bfloat16)
+    bt = synth.make_page_table(B, pages, B * pages, shuffle=True, device="cuda")
+    ids = torch.arange(B, dtype=torch.int32, device="cuda")
+    lens = torch.full((B,), ctx - R, dtype=torch.int32, device="cuda")
+    q = torch.randn((B * R, t.nq * t.hd), generator=g, device="cuda")
+    for _ in range(3):
+        binding.spec_attention(shape, pool, bt, 0, ids, lens, R, t.nq, 1, q)
+    torch.cuda.synchronize()
+
+
+CASES = {"projections": projections, "projections_wide": projections_wide, "projections_30b": projections_30b,
+         "projections_30b_m5": projections_30b_m5, "projections_wide_q4": projections_wide_q4,
+         "verify_q4b4": verify_q4b4, "draft": draft, "verify": verify, "attention_30b": attention_30b}
 
 
 def main(argv):
     if len(argv) != 1 or argv[0] not in CASES:
         print(__doc__)
         return 2
+    from speculative_decoding_spec_gb300 import build
+    build.build()
     CASES[argv[0]](configs.WORKLOADS[WORKLOAD])
     return 0
 

@@ -22,9 +22,9 @@ DTYPES = {F32: 0, BF16: 1, Q4_0: 2}
 EXPORTS = ["spec_workspace_bytes", "spec_init", "spec_prefill", "spec_draft", "spec_verify", "spec_step",
            "spec_decode", "spec_inject_drafts", "spec_stats", "spec_sync", "spec_set_graphs",
            "spec_kernel_launches", "spec_status_str", "spec_destroy", "spec_linear",
-           "spec_linear_workspace_bytes", "spec_linear_noalloc", "spec_set_option"]
-(SPEC_OPT_GRAPHS, SPEC_OPT_PERSISTENT, SPEC_OPT_TRACE, SPEC_OPT_PREFETCH, SPEC_OPT_DRAFT_CLUSTER,
- SPEC_OPT_DRAFT_TRACE) = 1, 2, 3, 4, 5, 6
+           "spec_linear_workspace_bytes", "spec_linear_noalloc", "spec_set_option",
+           "spec_attention_workspace_bytes", "spec_attention"]
+SPEC_OPT_GRAPHS, SPEC_OPT_PREFETCH, SPEC_OPT_TEST_ATTN_WAIT = 1, 4, 8
 SPEC_OPT_WIDE_TRACE = 7
 SPEC_LINEAR_NOALLOC_MAX_ROWS = 523776
 
@@ -120,6 +120,10 @@ def lib():
     L.spec_set_option.argtypes = [p, i32, C.c_int64]
     L.spec_linear_noalloc.restype = st
     L.spec_linear_noalloc.argtypes = [C.POINTER(spec_matrix), i32, i32, p, i32, p, C.c_float, p, p]
+    L.spec_attention_workspace_bytes.restype = C.c_size_t
+    L.spec_attention_workspace_bytes.argtypes = [p, i32, i32, i32, i32]
+    L.spec_attention.restype = st
+    L.spec_attention.argtypes = [p, p, i32, i32, p, p, i32, i32, i32, p, p, p, C.c_size_t, p]
     L.spec_destroy.restype = None
     L.spec_destroy.argtypes = [p]
     _lib = L
@@ -188,6 +192,31 @@ def spec_linear_noalloc(w, x: torch.Tensor, gain: Optional[torch.Tensor] = None,
     return y
 
 
+def spec_attention(t, pool: torch.Tensor, block_table: torch.Tensor, layer: int, seq_ids: torch.Tensor,
+                   seq_len: torch.Tensor, R: int, n_q_heads: int, key_extra: int, q: torch.Tensor,
+                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One attention launch over a paged cache (include/spec.h spec_attention).
+    pool [L][n_pages][2][nkv][64][hd] in the cache dtype of shape t,
+    block_table int32 [n_slots][max_pages], q float32 [B*R][n_q_heads*hd]."""
+    L = lib()
+    md = model_desc(t)
+    kv = spec_kv_desc(_ptr(pool), pool.shape[1], PAGE, _ptr(block_table), block_table.shape[1],
+                      block_table.shape[0])
+    B = seq_ids.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    nbytes = L.spec_attention_workspace_bytes(C.byref(md), B, R, n_q_heads, block_table.shape[1])
+    if nbytes == 0:
+        raise SpecError("spec_attention_workspace_bytes", SPEC_EINVAL)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=q.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    check("spec_attention", L.spec_attention(C.byref(md), C.byref(kv), layer, B, _ptr(seq_ids), _ptr(seq_len),
+                                             R, n_q_heads, key_extra, _ptr(q), _ptr(out), _ptr(ws), nbytes,
+                                             s.cuda_stream))
+    out.workspace = ws      # error word in its first int
+    return out
+
+
 _LINEAR_WS = {}
 
 
@@ -206,8 +235,7 @@ class Engine:
     around one spec_ctx and forwards calls to the C ABI on its own stream."""
 
     def __init__(self, tw, dw=None, n_slots=1, B_max=1, rows_max=4, max_ctx=256, shuffle_pages=False,
-                 device="cuda", graphs=True, persistent=False,
-                 draft_cluster=False):
+                 device="cuda", graphs=True):
         L = lib()
         t = tw.shape
         self.tw, self.dw, self.shape = tw, dw, t
@@ -253,8 +281,6 @@ class Engine:
         self.ctx = ctx
         if not graphs:
             check("spec_set_graphs", L.spec_set_graphs(ctx, 0))
-        check("spec_set_option", L.spec_set_option(ctx, SPEC_OPT_PERSISTENT, int(bool(persistent))))
-        check("spec_set_option", L.spec_set_option(ctx, SPEC_OPT_DRAFT_CLUSTER, int(bool(draft_cluster))))
         self._bufs = {}
 
     # -- helpers ------------------------------------------------------------

@@ -120,4 +120,4 @@ WORKLOADS = {
                                             ctx=(8192, 8192), k=4, alphas=(0.5, 0.8)),
 }
 
-BENCH_WORKLOAD = "e2b_bf16_b1_ctx2048_k3"
+BENCH_WORKLOAD = "dense30b_bf16_b8_ctx8192_k4"

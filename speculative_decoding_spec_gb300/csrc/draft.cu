@@ -29,10 +29,13 @@ SPEC_DEV float elem(const Mat& W, int K, long long row, int col) {
 }
 
 __global__ void commit_hidden_kernel(int B, const int32_t* seq_ids, const int32_t* sel_row, const float* x,
-                                     int d, const float* g, float eps, float* hid) {
+                                     int d, const float* g, float eps, float* hid, const int* err) {
   __shared__ float red[32];
   grid_dep_wait();
   grid_dep_launch();
+  // a pass that recorded a device error commits nothing (its tail left
+  // seq_len and pending as they were; the hidden state stays with them)
+  if (err && *(const volatile int*)err) return;
   const int b = blockIdx.x;
   const float* xr = x + (size_t)sel_row[b] * d;
   float ss = 0.f;
@@ -212,11 +215,11 @@ cudaLaunchConfig_t cfg_pdl(dim3 grid, dim3 block, size_t smem, cudaStream_t st, 
 }  // namespace
 
 int commit_hidden(int B, const int32_t* seq_ids, const int32_t* sel_row, const float* x, int d,
-                  const float* g_final, float eps, float* hid_state, cudaStream_t st) {
+                  const float* g_final, float eps, float* hid_state, const int* err, cudaStream_t st) {
   cudaLaunchAttribute at[1];
   cudaLaunchConfig_t cfg = cfg_pdl(dim3(B), dim3(256), 0, st, at);
-  return cudaLaunchKernelEx(&cfg, commit_hidden_kernel, B, seq_ids, sel_row, x, d, g_final, eps, hid_state) ==
-                 cudaSuccess ? 1 : -1;
+  return cudaLaunchKernelEx(&cfg, commit_hidden_kernel, B, seq_ids, sel_row, x, d, g_final, eps, hid_state,
+                            err) == cudaSuccess ? 1 : -1;
 }
 
 int draft_input(const DraftInArgs& a, cudaStream_t st) {
@@ -249,15 +252,17 @@ int inject_drafts(int B, int k, const int32_t* seq_ids, const int32_t* seq_len, 
                             offsets, vocab, err) == cudaSuccess ? 1 : -1;
 }
 
+// SM count of the current device (looked up once per device).
 int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+  static int n[MAX_DEVICES] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) dev = 0;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 148;
   }
-  return n;
+  return n[dev];
 }
 
 }  // namespace spec

@@ -158,8 +158,9 @@ struct AttnArgs {
 int attention(const AttnArgs& a, cudaStream_t st);
 
 // Final-normed hidden state of the row chosen by the accept step -> slot state.
+// Skipped when the device error word `err` is set (the pass commits nothing).
 int commit_hidden(int B, const int32_t* seq_ids, const int32_t* sel_row, const float* x, int d,
-                  const float* g_final, float eps, float* hid_state, cudaStream_t st);
+                  const float* g_final, float eps, float* hid_state, const int* err, cudaStream_t st);
 
 // Drafter step input: cat[b] = [N(h); N(E[tok])], RoPE table at the draft position.
 struct DraftInArgs {
@@ -194,53 +195,6 @@ struct ClusterArgs {
 };
 int cluster_head(const ClusterArgs& a, cudaStream_t st);
 
-// All k drafter steps of B sequences in one launch: one thread-block cluster
-// per sequence (draft_cluster.cu). The host fills the model, state and buffer
-// fields; draft_cluster_plan() fills the layout fields (ncta .. off_y).
-struct DraftDesc {
-  int B, k;
-  int d, h, L, dnq, nkv, hd, ff;      // target width; drafter width, layers, q heads, kv heads, ffn
-  int V, C, top_c, cs, clustered;     // vocabulary; centroids, clusters kept, cluster size
-  float eps, theta;
-  int wdtype, kv_dtype;
-  Mat embed;                          // target embedding [V][d]
-  Mat w_in, wq, wo, wgu, wdown, w_out, centroids, vocab;
-  const float *g_in_h, *g_in_e, *g_attn, *g_ffn, *g_out;
-  const int32_t* perm;                // [V] vocabulary row -> token id (clustered head)
-  const int32_t* seq_ids;             // [B]
-  const int32_t* seq_len;             // state [slots]
-  const int32_t* pending;             // state [slots]
-  const float* hid;                   // state [slots][d]
-  const void* pool;                   // KV pool
-  long long layer_off;                // elements to the target's last layer
-  int n_pages, max_pages;
-  const int32_t* block_table;         // [slots][max_pages]
-  float* part;                        // attention partials, part_stride floats per sequence (fp32 cache)
-  long long part_stride;
-  // tensor-core attention (bf16 cache): queries and RoPE rows in, output out
-  float* q;                           // [B][dnq*hd]
-  float* rope;                        // [B][hd]
-  float* att;                         // [B][dnq*hd]
-  float* part_o;                      // [B][dnq][ncta][hd] split partials
-  float* part_ml;                     // [B][dnq][ncta][2]
-  unsigned int* att_cnt;              // [B][nkv] arrival counters, zero between launches
-  long long layer_elems;              // pool elements per target layer
-  int tlayer;                         // the target's last layer
-  int32_t* drafts;                    // out [B][k]
-  int* err;
-  unsigned long long* trace;          // optional phase timestamps (sequence 0, CTA 0)
-  // layout (draft_cluster_plan)
-  int ncta, ns, pw_cap;
-  int off_u1, off_qaa, off_u, off_sc, off_part, off_y;
-  size_t smem;
-};
-// Fills the layout fields; false when the shapes are outside what the fused
-// drafter handles (the caller then runs the per-kernel drafter).
-bool draft_cluster_plan(DraftDesc& d);
-// Attention partial floats per sequence (any plan), G = q heads per kv head.
-long long draft_cluster_part_floats(int G, int hd);
-int draft_cluster(const DraftDesc& d, cudaStream_t st);
-
 int inject_drafts(int B, int k, const int32_t* seq_ids, const int32_t* seq_len, int32_t* drafts,
                   const int32_t* ref, int ref_len, float alpha, const float* draws,
                   const int32_t* offsets, int vocab, int* err, cudaStream_t st);
@@ -260,44 +214,12 @@ inline size_t gemv_wide_xs_bytes(int kmax) { return (size_t)2 * 64 * kmax * 2; }
 void setup_attn_attributes();
 void setup_draft_attributes();
 
+constexpr int MAX_DEVICES = 64;
 int num_sms();
+// Sets every kernel's dynamic shared-memory limit on the current device, once
+// per device (function attributes are per device). Call outside stream capture.
+void setup_device_attributes();
 
-// One target pass (prefill or verify) as a single persistent kernel: every
-// phase below runs on all SMs, separated by a grid barrier.
-struct PassDesc {
-  int L, d, nq, nkv, hd, ff, V;
-  float eps, theta;
-  Mat embed, wqkv, wo, wgu, wdown;
-  const float *g_attn, *g_ffn, *g_final;
-  void* pool;
-  long long layer_elems;
-  int n_pages, max_pages;
-  const int32_t* block_table;
-  int32_t *seq_len, *pending;
-  float* hid;
-  int64_t* stats;
-  int B, R, mode;
-  const int32_t* seq_ids;
-  const int32_t* tokens;
-  int32_t *out_tokens, *n_emitted;
-  float* logits;
-  float *x, *qkv, *att, *act, *part_o, *part_ml, *rope_cs;
-  int32_t *pos, *sel_row;
-  unsigned long long* best;
-  unsigned int *counter, *attn_cnt, *tc_cnt, *bar;
-  float* tc_fix;
-  int* err;
-  int* abort_flag;
-  int nsm, n_split, pps;
-  unsigned long long* trace;  // optional [steps][nsm][6] globaltimer marks
-  size_t smem_bytes;          // dynamic shared memory of the launch (set by the launcher)
-  int prefetch;               // pull the next step's weights / pages to L2 before each barrier
-};
-// Launches the persistent pass kernel (cooperative). Returns 1, or -2 when
-// the device cannot hold the whole grid at once (caller uses per-phase
-// kernels), or -1 on a launch error.
-int pass_persistent(const PassDesc& d, cudaStream_t st);
-bool pass_persistent_supported(int hd, int max_rows);
 // tensor-core attention for bf16 caches (head_dim 64 or 128)
 size_t attention_tc_smem(int hd, int qn, int r);
 size_t attention_tc_smem_slots(int hd, int qn, int r, int pw);
@@ -305,5 +227,13 @@ void setup_attn_tc_attributes();
 int attention_tc_splits(int B, int nkv, int max_pages, int* pps, int qn);
 int attention_tc(const AttnArgs& a, unsigned int* counters, int pps, cudaStream_t st);
 size_t attention_smem(int hd, int qn);
+// tcgen05 attention (attn_flash.cu): bf16 cache, head_dim 128, at most 32
+// query rows (R x GQA group) per (sequence, KV head). counters: 2 x B x nkv
+// words, zero between launches. wait_extra > 0 makes the split merge's
+// bounded wait run out (failure-detection tests only). Returns 1, -2 when the
+// shape is not covered, -1 on a launch error.
+void setup_attn_flash_attributes();
+bool attention_flash_ok(const AttnArgs& a);
+int attention_flash(const AttnArgs& a, unsigned int* counters, int wait_extra, cudaStream_t st);
 
 }  // namespace spec

@@ -30,7 +30,7 @@ constexpr size_t SCRATCH_BYTES = FIX_BYTES + CNT_BYTES;
 
 static __device__ __align__(256) unsigned char g_linear_scratch[SCRATCH_BYTES];
 
-constexpr int MAX_DEVICES = 64;
+using spec::MAX_DEVICES;
 std::mutex g_mu;
 void* g_addr[MAX_DEVICES] = {};
 
@@ -71,8 +71,7 @@ extern "C" spec_status spec_linear_noalloc(const spec_matrix* w, int32_t N, int3
   cudaStream_t st = (cudaStream_t)stream;
   unsigned int* cnt = (unsigned int*)((char*)base + FIX_BYTES);
   if (cudaMemsetAsync(cnt, 0, cnt_bytes, st) != cudaSuccess) return SPEC_ECUDA;
-  static std::once_flag once;
-  std::call_once(once, spec::setup_gemv_attributes);
+  spec::setup_device_attributes();
   spec::GemvArgs g = {};
   g.X = x; g.ldx = K; g.M = M; g.N = N; g.K = K;
   g.W = spec::Mat{w->dtype, w->data, w->scales};

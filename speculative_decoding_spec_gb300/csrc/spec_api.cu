@@ -35,17 +35,12 @@ struct Work {
   unsigned long long* best;
   unsigned int* counter;
   unsigned int* attn_count;
-  unsigned int* bar;
-  int* abort_flag;
   float* tc_fix;
   unsigned int* tc_cnt;
   WideScratch wide;         // tcgen05 projection scratch (null when passes have <= 8 rows)
   int* err;
   // drafter
   float *d_cat, *d_u, *d_q, *d_att, *d_act, *d_h, *d_scores, *d_rope, *d_part_o, *d_part_ml;
-  float* d_cpart;           // fused drafter: attention partials (fp32 cache)
-  float *d_cpo, *d_cpml;    // fused drafter: tensor-core attention split partials
-  unsigned int* d_ccnt;     // fused drafter: attention arrival counters
   int32_t *d_chosen, *d_drafts;
   unsigned long long* d_best;
   unsigned int* d_counter;
@@ -83,9 +78,7 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
   w.n_emit1 = b.take<int32_t>(base, B_max);
   w.best = b.take<unsigned long long>(base, M);
   w.counter = b.take<unsigned int>(base, 4);
-  w.attn_count = b.take<unsigned int>(base, (size_t)B_max * m.n_kv_heads);
-  w.bar = b.take<unsigned int>(base, 4);
-  w.abort_flag = b.take<int>(base, 4);
+  w.attn_count = b.take<unsigned int>(base, (size_t)2 * B_max * m.n_kv_heads);
   w.tc_fix = b.take<float>(base, gemv_tc_fixup_bytes() / sizeof(float));
   w.tc_cnt = b.take<unsigned int>(base, tc_counters(m, d));
   w.err = b.take<int>(base, 4);
@@ -115,11 +108,6 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
     w.d_drafts = b.take<int32_t>(base, (size_t)B_max * KMAX);
     w.d_best = b.take<unsigned long long>(base, B_max);
     w.d_counter = b.take<unsigned int>(base, 4);
-    w.d_cpart = b.take<float>(base, (size_t)B_max *
-                                        draft_cluster_part_floats(d->n_q_heads / m.n_kv_heads, m.head_dim));
-    w.d_cpo = b.take<float>(base, (size_t)B_max * d->n_q_heads * 16 * m.head_dim);
-    w.d_cpml = b.take<float>(base, (size_t)B_max * d->n_q_heads * 16 * 2);
-    w.d_ccnt = b.take<unsigned int>(base, (size_t)B_max * m.n_kv_heads);
   }
   w.bytes = (b.off + 255) & ~size_t(255);
   return w;
@@ -169,15 +157,10 @@ struct spec_ctx {
   Work wk;
   bool graphs = true;
   bool fused_rope = false;
-  bool persistent = false;
-  unsigned long long* trace = nullptr;
   bool prefetch = false;
-  bool draft_cluster = false;
-  unsigned long long* dtrace = nullptr;
+  int test_attn_wait = 0;   // SPEC_OPT_TEST_ATTN_WAIT
   unsigned long long* wtrace = nullptr;  // tcgen05 projection timelines (SPEC_OPT_WIDE_TRACE)
   int wtrace_n = 0;
-  int cluster_plan = 0;     // fused drafter layout: 0 not made yet, 1 made, -1 not supported
-  DraftDesc cplan;
   long long launches = 0;
   struct Entry {
     cudaGraphExec_t exec;
@@ -194,18 +177,62 @@ int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st);
 int kv_dt(const spec_ctx* c) { return c->m.kv_dtype == SPEC_F32 ? DT_F32 : DT_BF16; }
 
 // Tensor-core attention for bf16 caches with head_dim 64/128; the CUDA-core
-// kernels otherwise (fp32 caches).
-int run_attention(spec_ctx* c, AttnArgs at, cudaStream_t st) {
-  if (c->m.kv_dtype == SPEC_BF16 && (c->m.head_dim == 64 || c->m.head_dim == 128)) {
+// kernels otherwise (fp32 caches). `counters` [B][nkv] are zero between
+// launches; the partial buffers of `at` hold max_pages splits per row and head.
+int launch_attention(int kv_dtype, AttnArgs at, unsigned int* counters, int wait_extra, cudaStream_t st) {
+  if (kv_dtype == SPEC_BF16 && attention_flash_ok(at)) return attention_flash(at, counters, wait_extra, st);
+  if (kv_dtype == SPEC_BF16 && (at.hd == 64 || at.hd == 128)) {
     int pps = 1;
-    at.n_split = attention_tc_splits(at.B, at.nkv, c->kv.max_pages_per_seq, &pps, at.R * (at.nq / at.nkv));
+    at.n_split = attention_tc_splits(at.B, at.nkv, at.max_pages, &pps, at.R * (at.nq / at.nkv));
     at.pages_per_split = pps;
-    const int r = attention_tc(at, c->wk.attn_count, pps, st);
+    const int r = attention_tc(at, counters, pps, st);
     if (r != -2) return r;
-    at.n_split = c->kv.max_pages_per_seq;  // the CUDA-core kernel's split: one page each
+    at.n_split = at.max_pages;  // the CUDA-core kernel's split: one page each
     at.pages_per_split = 1;
   }
   return attention(at, st);
+}
+
+int run_attention(spec_ctx* c, AttnArgs at, cudaStream_t st) {
+  return launch_attention(c->m.kv_dtype, at, c->wk.attn_count, c->test_attn_wait, st);
+}
+
+}  // namespace
+
+void spec::setup_device_attributes() {
+  static std::mutex mu;
+  static bool done[MAX_DEVICES];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) dev = 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev]) return;
+  setup_gemv_attributes();
+  setup_attn_attributes();
+  setup_attn_tc_attributes();
+  setup_draft_attributes();
+  setup_attn_flash_attributes();
+  done[dev] = true;
+}
+
+namespace {
+
+// Workspace of spec_attention: error word, arrival counters, split partials.
+struct AttnWork {
+  int* err;
+  unsigned int* counters;
+  float *part_o, *part_ml;
+  size_t bytes;
+};
+AttnWork carve_attention(char* base, int B, int R, int nq, int nkv, int hd, int max_pages) {
+  AttnWork w = {};
+  Buf b;
+  const size_t M = (size_t)B * R;
+  w.err = b.take<int>(base, 4);
+  w.counters = b.take<unsigned int>(base, (size_t)2 * B * nkv);
+  w.part_o = b.take<float>(base, M * nq * (size_t)max_pages * hd);
+  w.part_ml = b.take<float>(base, M * nq * (size_t)max_pages * 2);
+  w.bytes = (b.off + 255) & ~size_t(255);
+  return w;
 }
 
 // ---- the target pass: rows -> layers -> LM head + argmax + accept -----------
@@ -222,27 +249,6 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     if (r < 0) return -1;   \
     n += r;                 \
   } while (0)
-
-  if (c->persistent && c->fused_rope && m.w_dtype == SPEC_BF16 && pass_persistent_supported(hd, M)) {
-    PassDesc D = {};
-    D.L = m.n_layers; D.d = d; D.nq = nq; D.nkv = nkv; D.hd = hd; D.ff = ff; D.V = m.vocab;
-    D.eps = m.rms_eps; D.theta = m.rope_theta;
-    D.embed = M_(c->w.embed); D.wqkv = M_(c->w.wqkv); D.wo = M_(c->w.wo); D.wgu = M_(c->w.wgu);
-    D.wdown = M_(c->w.wdown); D.g_attn = c->w.g_attn; D.g_ffn = c->w.g_ffn; D.g_final = c->w.g_final;
-    D.pool = c->kv.pool; D.layer_elems = c->layer_elems; D.n_pages = c->kv.n_pages;
-    D.max_pages = c->kv.max_pages_per_seq; D.block_table = c->kv.block_table;
-    D.seq_len = c->state.seq_len; D.pending = c->state.pending; D.hid = c->state.hid; D.stats = c->state.stats;
-    D.B = B; D.R = R; D.mode = mode; D.seq_ids = seq_ids; D.tokens = tokens; D.out_tokens = out_tokens;
-    D.n_emitted = n_emitted; D.logits = logits;
-    D.x = w.x; D.qkv = w.qkv; D.att = w.att; D.act = w.act; D.part_o = w.part_o; D.part_ml = w.part_ml;
-    D.rope_cs = w.rope_cs; D.pos = w.pos; D.sel_row = w.sel_row; D.best = w.best; D.counter = w.counter;
-    D.attn_cnt = w.attn_count; D.tc_cnt = w.tc_cnt; D.bar = w.bar; D.tc_fix = w.tc_fix; D.err = w.err;
-    D.abort_flag = w.abort_flag; D.nsm = num_sms(); D.trace = c->trace; D.prefetch = c->prefetch;
-    D.n_split = attention_tc_splits(B, nkv, c->kv.max_pages_per_seq, &D.pps, R * (nq / nkv));
-    r = pass_persistent(D, st);
-    if (r == -1) return -1;
-    if (r > 0) return r;
-  }
 
   RowsArgs ra = {};
   ra.B = B; ra.R = R; ra.mode = mode; ra.seq_ids = seq_ids; ra.tokens = tokens;
@@ -316,50 +322,11 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
   t.pending = c->state.pending; t.stats = c->state.stats; t.sel_row = w.sel_row;
   t.best_all = w.best; t.counter = w.counter; t.err = w.err;
   LAUNCH(run_gemv(c, g, st));
-  LAUNCH(commit_hidden(B, seq_ids, w.sel_row, w.x, d, c->w.g_final, m.rms_eps, c->state.hid, st));
+  LAUNCH(commit_hidden(B, seq_ids, w.sel_row, w.x, d, c->w.g_final, m.rms_eps, c->state.hid, w.err, st));
   return n;
 }
 
 // ---- the drafter: k autoregressive steps on the target's last hidden state ---
-// The fused drafter's description for this context (layout planned once).
-bool cluster_desc(spec_ctx* c, DraftDesc& D) {
-  if (c->cluster_plan == 0) {
-    const spec_model_desc& m = c->m;
-    const spec_drafter_desc& dd = c->dd;
-    const spec_drafter_weights& dw = c->dw;
-    DraftDesc P = {};
-    P.B = 1; P.k = 1;
-    P.d = m.d_model; P.h = dd.hidden; P.L = dd.n_layers; P.dnq = dd.n_q_heads; P.nkv = m.n_kv_heads;
-    P.hd = m.head_dim; P.ff = dd.d_ff; P.V = m.vocab; P.clustered = dd.clustered;
-    P.C = dd.clustered ? dd.n_centroids : 0; P.top_c = dd.top_c;
-    P.cs = dd.clustered ? m.vocab / dd.n_centroids : 0;
-    P.eps = m.rms_eps; P.theta = m.rope_theta; P.wdtype = dd.w_dtype; P.kv_dtype = kv_dt(c);
-    P.embed = M_(c->w.embed);
-    P.w_in = M_(dw.w_in); P.wq = M_(dw.wq); P.wo = M_(dw.wo); P.wgu = M_(dw.wgu); P.wdown = M_(dw.wdown);
-    P.w_out = M_(dw.w_out); P.centroids = M_(dw.centroids); P.vocab = M_(dw.vocab);
-    P.g_in_h = dw.g_in_h; P.g_in_e = dw.g_in_e; P.g_attn = dw.g_attn; P.g_ffn = dw.g_ffn; P.g_out = dw.g_out;
-    P.perm = dw.perm;
-    P.seq_len = c->state.seq_len; P.pending = c->state.pending; P.hid = c->state.hid;
-    P.pool = c->kv.pool; P.layer_off = (long long)(m.n_layers - 1) * c->layer_elems;
-    P.n_pages = c->kv.n_pages; P.max_pages = c->kv.max_pages_per_seq; P.block_table = c->kv.block_table;
-    P.part = c->wk.d_cpart; P.err = c->wk.err;
-    P.q = c->wk.d_q; P.rope = c->wk.d_rope; P.att = c->wk.d_att; P.part_o = c->wk.d_cpo;
-    P.part_ml = c->wk.d_cpml; P.att_cnt = c->wk.d_ccnt; P.layer_elems = c->layer_elems;
-    P.tlayer = m.n_layers - 1;
-    // every matrix the bulk copies read must start 16-byte aligned
-    bool aligned = true;
-    for (const spec_matrix* mm : {&dw.w_in, &dw.wq, &dw.wo, &dw.wgu, &dw.wdown, &dw.w_out, &dw.vocab})
-      aligned = aligned && ((uintptr_t)mm->data % 16 == 0) && ((uintptr_t)mm->scales % 16 == 0);
-    if (dd.clustered)
-      aligned = aligned && ((uintptr_t)dw.centroids.data % 16 == 0) && ((uintptr_t)dw.centroids.scales % 16 == 0);
-    c->cluster_plan = aligned && draft_cluster_plan(P) ? 1 : -1;
-    c->cplan = P;
-  }
-  if (c->cluster_plan != 1) return false;
-  D = c->cplan;
-  return true;
-}
-
 int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* drafts, cudaStream_t st) {
   const spec_model_desc& m = c->m;
   const spec_drafter_desc& dd = c->dd;
@@ -367,11 +334,6 @@ int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* dr
   const Work& w = c->wk;
   const int d = m.d_model, h = dd.hidden, hd = m.head_dim, dq = dd.n_q_heads * hd, ff = dd.d_ff;
   int n = 0, r;
-  DraftDesc D;
-  if (c->draft_cluster && cluster_desc(c, D)) {
-    D.B = B; D.k = k; D.seq_ids = seq_ids; D.drafts = drafts; D.trace = c->dtrace;
-    return draft_cluster(D, st);
-  }
   for (int j = 1; j <= k; ++j) {
     DraftInArgs di = {};
     di.B = B; di.j = j; di.k = k; di.d = d; di.hd = hd; di.seq_ids = seq_ids;
@@ -574,10 +536,7 @@ spec_status spec_init(const spec_model_desc* model, const spec_weights* weights,
   c->rows_max = rows_max;
   c->layer_elems = (long long)kv->n_pages * 2 * m.n_kv_heads * 64 * m.head_dim;
   c->wk = carve((char*)workspace, m, drafter, B_max, rows_max, kv->max_pages_per_seq);
-  setup_gemv_attributes();
-  setup_attn_attributes();
-  setup_attn_tc_attributes();
-  setup_draft_attributes();
+  setup_device_attributes();
   // RoPE and the KV append run in the QKV projection's epilogue when that
   // projection is the tensor-core kernel (bf16 or Q4_0) writing a bf16 cache
   c->fused_rope = ((m.w_dtype == SPEC_BF16 && m.d_model % 32 == 0) ||
@@ -587,12 +546,6 @@ spec_status spec_init(const spec_model_desc* model, const spec_weights* weights,
   if (cudaMemsetAsync(workspace, 0, need.bytes, st) != cudaSuccess) {
     delete c;
     return SPEC_ECUDA;
-  }
-  if (c->has_drafter) {
-    // lay out the fused drafter now: planning queries the device, which a
-    // stream capture in progress must not see
-    DraftDesc D;
-    cluster_desc(c, D);
   }
   *out = c;
   return SPEC_OK;
@@ -683,9 +636,43 @@ spec_status spec_linear(const spec_matrix* w, int32_t N, int32_t K, const float*
     g.wide.rms = (float*)p;
     g.wide.kmax = K;
   }
-  static std::once_flag once;
-  std::call_once(once, setup_gemv_attributes);
+  setup_device_attributes();
   if (gemv(g, (cudaStream_t)stream) < 0) return SPEC_ECUDA;
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+size_t spec_attention_workspace_bytes(const spec_model_desc* m, int32_t B, int32_t R, int32_t n_q_heads,
+                                      int32_t max_pages_per_seq) {
+  if (!m || !model_ok(*m) || B <= 0 || R <= 0 || n_q_heads <= 0 || n_q_heads % m->n_kv_heads ||
+      max_pages_per_seq <= 0)
+    return 0;
+  return carve_attention(nullptr, B, R, n_q_heads, m->n_kv_heads, m->head_dim, max_pages_per_seq).bytes;
+}
+
+spec_status spec_attention(const spec_model_desc* m, const spec_kv_desc* kv, int32_t layer, int32_t B,
+                           const int32_t* seq_ids, const int32_t* seq_len, int32_t R, int32_t n_q_heads,
+                           int32_t key_extra, const float* q, float* out, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  if (!m || !model_ok(*m) || !kv || !kv->pool || !kv->block_table || kv->page_size != 64 || kv->n_pages <= 0 ||
+      kv->max_pages_per_seq <= 0 || layer < 0 || layer >= m->n_layers || B <= 0 || B > 64 || !seq_ids ||
+      !seq_len || R <= 0 || R > 64 || n_q_heads <= 0 || n_q_heads % m->n_kv_heads || (key_extra != 0 && key_extra != 1) ||
+      !q || !out || !workspace)
+    return SPEC_EINVAL;
+  if (R * (n_q_heads / m->n_kv_heads) > 128) return SPEC_EUNSUPPORTED;
+  const AttnWork w = carve_attention((char*)workspace, B, R, n_q_heads, m->n_kv_heads, m->head_dim,
+                                     kv->max_pages_per_seq);
+  if (ws_bytes < w.bytes) return SPEC_ECAPACITY;
+  AttnArgs at = {};
+  at.q = q; at.ldq = n_q_heads * m->head_dim; at.B = B; at.R = R; at.nq = n_q_heads; at.nkv = m->n_kv_heads;
+  at.hd = m->head_dim; at.key_extra = key_extra; at.pool = kv->pool;
+  at.kv_dtype = m->kv_dtype == SPEC_F32 ? DT_F32 : DT_BF16;
+  at.layer_elems = (long long)kv->n_pages * 2 * m->n_kv_heads * 64 * m->head_dim;
+  at.layer = layer; at.n_pages = kv->n_pages; at.max_pages = kv->max_pages_per_seq;
+  at.block_table = kv->block_table; at.seq_ids = seq_ids; at.seq_len = seq_len; at.rope_cs = nullptr;
+  at.n_split = kv->max_pages_per_seq; at.pages_per_split = 1; at.part_o = w.part_o; at.part_ml = w.part_ml;
+  at.out = out; at.err = w.err;
+  setup_device_attributes();
+  if (launch_attention(m->kv_dtype, at, w.counters, 0, (cudaStream_t)stream) < 0) return SPEC_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
 
@@ -712,13 +699,7 @@ spec_status spec_sync(spec_ctx* c, void* stream) {
   if (cudaMemcpy(&err, c->wk.err, sizeof err, cudaMemcpyDeviceToHost) != cudaSuccess) return SPEC_ECUDA;
   if (err) {
     if (cudaMemset(c->wk.err, 0, sizeof(int)) != cudaSuccess) return SPEC_ECUDA;
-    if (err == SPEC_ERR_TIMEOUT) {
-      // a bounded wait gave up: reset the barrier state so the next pass can run
-      if (cudaMemset(c->wk.bar, 0, 4 * sizeof(unsigned int)) != cudaSuccess ||
-          cudaMemset(c->wk.abort_flag, 0, sizeof(int)) != cudaSuccess)
-        return SPEC_ECUDA;
-      return SPEC_ETIMEOUT;
-    }
+    if (err == SPEC_ERR_TIMEOUT) return SPEC_ETIMEOUT;
     return err == SPEC_ERR_CAPACITY ? SPEC_ECAPACITY : SPEC_EINVAL;
   }
   return SPEC_OK;
@@ -734,11 +715,8 @@ spec_status spec_set_option(spec_ctx* c, int32_t option, int64_t value) {
   if (!c) return SPEC_EINVAL;
   std::lock_guard<std::mutex> lk(c->mu);
   if (option == SPEC_OPT_GRAPHS) c->graphs = value != 0;
-  else if (option == SPEC_OPT_PERSISTENT) c->persistent = value != 0;
-  else if (option == SPEC_OPT_TRACE) c->trace = (unsigned long long*)(uintptr_t)value;
   else if (option == SPEC_OPT_PREFETCH) c->prefetch = value != 0;
-  else if (option == SPEC_OPT_DRAFT_CLUSTER) c->draft_cluster = value != 0;
-  else if (option == SPEC_OPT_DRAFT_TRACE) c->dtrace = (unsigned long long*)(uintptr_t)value;
+  else if (option == SPEC_OPT_TEST_ATTN_WAIT) c->test_attn_wait = value > 0 ? 1 : 0;
   else if (option == SPEC_OPT_WIDE_TRACE) {
     c->wtrace = (unsigned long long*)(uintptr_t)value;
     c->wtrace_n = 0;

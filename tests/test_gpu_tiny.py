@@ -37,14 +37,14 @@ def models(request):
     return tw, dw, T, D, prompt, s0
 
 
-def _engine(tw, dw, graphs=True, persistent=False, draft_cluster=False):
+def _engine(tw, dw, graphs=True):
     return binding.Engine(tw, dw, n_slots=2, B_max=2, rows_max=64, max_ctx=CAP, shuffle_pages=True,
-                          graphs=graphs, persistent=persistent, draft_cluster=draft_cluster)
+                          graphs=graphs)
 
 
-def _prefilled(models, graphs=True, persistent=False, draft_cluster=False):
+def _prefilled(models, graphs=True):
     tw, dw, T, D, prompt, s0 = models
-    eng = _engine(tw, dw, graphs, persistent, draft_cluster)
+    eng = _engine(tw, dw, graphs)
     ids = eng.seq_ids([1])
     eng.spec_prefill(ids, eng._in("prompt", prompt.view(1, -1).cuda()))
     eng.sync()
@@ -81,16 +81,15 @@ def test_prefill_matches_oracle(models):
     assert_rows_close(eng.hid[1:2].cpu().numpy(), s0.hid[None], TOL[tw.shape.wdtype], "prefill hidden")
 
 
-@pytest.mark.parametrize("graphs,persistent", [(True, False), (False, False), (True, True)])
-def test_verify_logits_and_accept_match_oracle(models, graphs, persistent):
-    """Verify pass logits and accepted tokens, per-kernel (with and without
-    graphs) and as one persistent kernel per pass."""
+@pytest.mark.parametrize("graphs", [True, False])
+def test_verify_logits_and_accept_match_oracle(models, graphs):
+    """Verify pass logits and accepted tokens, with and without CUDA graphs."""
     tw, dw, T, D, prompt, s0 = models
-    eng, ids = _prefilled(models, graphs, persistent)
+    eng, ids = _prefilled(models, graphs)
     eng.close()
     G, _ = oracle.greedy(T, s0.clone(), 8)
     for drafts in ([G[0], G[1], 7], [G[0], G[1], G[2]], [5, 6, 7]):
-        eng2, ids2 = _prefilled(models, graphs, persistent)
+        eng2, ids2 = _prefilled(models, graphs)
         d = eng2._in("drafts", torch.tensor([drafts], dtype=torch.int32).cuda())
         logits = torch.empty((4, W.target.V), dtype=torch.float32, device="cuda")
         out, ne = eng2.spec_verify(ids2, d, logits)
@@ -120,9 +119,8 @@ def test_greedy_decode_matches_oracle(models):
     assert n >= 1
 
 
-@pytest.mark.parametrize("alpha,persistent", [(0.0, False), (0.5, False), (0.8, False), (1.0, False),
-                                              (0.5, True)])
-def test_speculative_output_equals_greedy(models, alpha, persistent):
+@pytest.mark.parametrize("alpha", [0.0, 0.5, 0.8, 1.0])
+def test_speculative_output_equals_greedy(models, alpha):
     """The pages' invariant on the GPU: tokens emitted by speculative steps
     equal plain greedy decoding, bit for bit (same kernels, row results that
     do not depend on the number of verified rows), and the oracle's greedy
@@ -139,7 +137,7 @@ def test_speculative_output_equals_greedy(models, alpha, persistent):
     # ref[slot][pos] = token at absolute position pos (pending sits at 64)
     ref[1, 64] = int(s0.pending)
     ref[1, 65:65 + len(greedy)] = torch.tensor(greedy, dtype=torch.int32)
-    eng2, ids2 = _prefilled(models, persistent=persistent)
+    eng2, ids2 = _prefilled(models)
     draws = synth.make_alpha_draws(steps * k, device="cuda")
     offs = synth.make_wrong_offsets(steps * k, W.target.V, device="cuda")
     emitted, per_step = [], []
@@ -166,32 +164,14 @@ def test_speculative_output_equals_greedy(models, alpha, persistent):
     assert st.accepted == st.emitted - st.passes and st.drafted == steps * k
 
 
-@pytest.mark.parametrize("draft_cluster", [True, False])
-def test_drafter_matches_oracle(models, draft_cluster):
-    """The k drafted tokens, from the fused one-cluster drafter and from the
-    one-kernel-per-operation drafter."""
+def test_drafter_matches_oracle(models):
+    """The k drafted tokens against the oracle's drafter (margin rule)."""
     tw, dw, T, D, prompt, s0 = models
-    eng, ids = _prefilled(models, draft_cluster=draft_cluster)
+    eng, ids = _prefilled(models)
     d = eng.spec_draft(ids, 1, W.k)
     eng.sync()
     ref, mg = oracle.draft(T, D, s0.clone(), W.k)
     compare_tokens(d[0].cpu().numpy(), ref, mg)
-
-
-def test_fused_drafter_is_one_launch(models):
-    """With fp32 or bf16 weights the tiny drafter runs as one kernel launch per
-    draft call (Q4_0 needs every reduction width to be a multiple of 256 and
-    falls back to the per-operation kernels at width 64)."""
-    tw, dw, T, D, prompt, s0 = models
-    eng, ids = _prefilled(models, graphs=False, draft_cluster=True)
-    before = eng.kernel_launches()
-    eng.spec_draft(ids, 1, W.k)
-    eng.sync()
-    n = eng.kernel_launches() - before
-    if tw.shape.wdtype == configs.Q4_0:
-        assert n > 1
-    else:
-        assert n == 1
 
 
 def test_step_emits_greedy_tokens(models):

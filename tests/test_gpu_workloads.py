@@ -3,12 +3,26 @@ targets with the 4-layer clustered drafter), through the C ABI.
 
 Each long context is a synthetic cache for positions [0, ctx-1) followed by
 one real target pass at ctx-1 (spec_prefill with R = 1), on the GPU and in the
-oracle alike. The oracle then checks, on the same inputs: the pending token
-and hidden state, the drafter's k tokens (margin rule), the verify pass's
-logits for every row (relative tolerance) and its emitted tokens. Batched
-workloads check a sample of sequences in the oracle (rows are independent).
+oracle alike. For every workload the oracle then checks, on the same inputs
+and for a sample of the batch's sequences (rows are independent):
+
+* the pending token and hidden state after that pass;
+* the drafter's k tokens (margin rule);
+* the verify pass's logits for every row (relative tolerance) and its emitted
+  tokens;
+* several further speculative steps (drafts injected at the workload's
+  acceptance rate): the tokens the GPU emitted over all steps must be the
+  oracle's own free-running greedy decode from the same state (up to 12
+  tokens for the ~30B-class model, all of them otherwise); a disagreement is
+  allowed only at an oracle margin <= 0.05, and the comparison stops there.
+The oracle runs only on its own inputs: where a GPU draft differs from the
+oracle's (an allowed near-tie flip) the verify comparison of that sequence is
+skipped rather than fed the GPU's draft.
+
 On the GPU alone, speculative steps at the workload's acceptance rate must
-emit exactly the GPU's plain greedy tokens."""
+emit exactly the GPU's plain greedy tokens ("Gemma 4's MTP drafter explained"
+(molayo1419.me), "How does speculative decoding work?": the output equals
+plain greedy decoding of the target)."""
 import numpy as np
 import pytest
 import torch
@@ -19,15 +33,16 @@ from tests.parity import TOL, assert_rows_close, compare_tokens
 
 pytestmark = pytest.mark.gpu
 
+STEPS = 4
 
-def _setup(w, steps_extra=64, persistent=False, draft_cluster=False):
+
+def _setup(w, steps_extra=64):
     t = w.target
     tw = synth.make_target(t, device="cuda")
     dw = synth.make_drafter(w.drafter, device="cuda")
     ctx = synth.make_context_lengths(w.B, *w.ctx)
     eng = binding.Engine(tw, dw, n_slots=w.B, B_max=w.B, rows_max=w.k + 1, max_ctx=max(ctx) + steps_extra,
-                         shuffle_pages=True, persistent=persistent,
-                         draft_cluster=draft_cluster)
+                         shuffle_pages=True)
     kvs = []
     for b in range(w.B):
         kv = synth.make_prefilled_kv(t, ctx[b] - 1, device="cuda", seed=synth.SEED_KV + b)
@@ -40,59 +55,10 @@ def _setup(w, steps_extra=64, persistent=False, draft_cluster=False):
     return tw, dw, eng, ids, ctx, kvs, first.cpu()
 
 
-@pytest.mark.parametrize("name,sample,persistent,draft_cluster", [
-    ("e2b_bf16_b1_ctx2048_k3", [0], False, False),
-    ("e2b_bf16_b1_ctx2048_k3", [0], True, True),
-    ("e2b_q4_0_b1_ctx4096_k4", [0], False, True),
-    ("e2b_q4_0_b4_ctx4096_k4", [1, 3], False, False),
-    ("e2b_q4_0_b4_ctx4096_k4", [2], False, True),
-    ("e4b_bf16_b8_ragged_k4", [0, 5], False, False),
-    ("e4b_bf16_b8_ragged_k4", [3], False, True),
-])
-def test_workload_matches_oracle(name, sample, persistent, draft_cluster):
-    w = configs.WORKLOADS[name]
-    t = w.target
-    tw, dw, eng, ids, ctx, kvs, first = _setup(w, persistent=persistent, draft_cluster=draft_cluster)
-    # GPU: draft, then verify the drafted rows with full logits
-    d = eng.spec_draft(ids, w.B, w.k).clone()
-    logits = torch.empty((w.B * (w.k + 1), t.V), dtype=torch.float32, device="cuda")
-    eng.sync()
-    pend = eng.pending.clone().cpu()
-    hid = eng.hid.clone().cpu()
-    out, ne = eng.spec_verify(ids, d, logits)
-    eng.sync()
-    T, D = oracle.Target(tw), oracle.Drafter(dw)
-    tol = TOL[t.wdtype]
-    for b in sample:
-        s = oracle.Seq(T, ctx[b] + w.k + 8)
-        s.load_prefilled(kvs[b].cpu())
-        oracle.prefill(T, s, first[b].numpy())
-        assert int(pend[b]) == s.pending
-        assert_rows_close(hid[b:b + 1].numpy(), s.hid[None], tol, "%s seq %d hidden" % (name, b))
-        ref_d, mg_d = oracle.draft(T, D, s.clone(), w.k)
-        compare_tokens(d[b].cpu().numpy(), ref_d, mg_d)
-        drafts = d[b].cpu().numpy()
-        am, mg, _, lg = oracle.forward(T, s.clone(), [s.pending] + list(drafts), want_logits=True)
-        rows = logits[b * (w.k + 1):(b + 1) * (w.k + 1)].cpu().numpy()
-        assert_rows_close(rows, lg, tol, "%s seq %d verify logits" % (name, b))
-        em, _ = oracle.verify(T, s, drafts)
-        n = int(ne[b])
-        compare_tokens(out[b, :n].cpu().numpy(), em, mg)
-        if np.all(mg[:len(em)] > 0.05):
-            assert n == len(em)
-
-
-@pytest.mark.parametrize("name", sorted(configs.WORKLOADS))
-def test_speculative_equals_greedy_on_gpu(name):
-    """Speculative steps with drafts injected at the workload's acceptance rate
-    emit exactly the tokens of the GPU's own plain greedy decoding."""
-    w = configs.WORKLOADS[name]
-    if w.prompt:
-        pytest.skip("covered by the tiny end-to-end tests")
-    steps = 4
-    tw, dw, eng, ids, ctx, kvs, first = _setup(w, steps_extra=(steps + 2) * (w.k + 1) + 64)
+def _gpu_greedy_ref(eng, ids, w, n_ref):
+    """GPU plain greedy tokens for every absolute position ahead (the draft
+    source of the acceptance injection); the slot state is restored."""
     saved = [x.clone() for x in (eng.seq_len, eng.pending, eng.hid, eng.stats)]
-    n_ref = steps * (w.k + 1) + w.k + 2
     start = eng.seq_len.clone()
     toks = [eng.pending.clone()]
     for _ in range(n_ref):
@@ -101,13 +67,14 @@ def test_speculative_equals_greedy_on_gpu(name):
     greedy = torch.stack(toks, 1).cpu()                     # [B][n_ref+1], from the pending token
     for dst, src in zip((eng.seq_len, eng.pending, eng.hid, eng.stats), saved):
         dst.copy_(src)
-    ref_len = int(start.max()) + n_ref + 8
-    ref = torch.zeros((w.B, ref_len), dtype=torch.int32)
+    ref = torch.zeros((w.B, int(start.max()) + n_ref + 8), dtype=torch.int32)
     for b in range(w.B):
         ref[b, int(start[b]):int(start[b]) + greedy.shape[1]] = greedy[b]
-    ref = ref.cuda()
-    alpha = w.alphas[-1] if w.alphas else 0.5
-    draws = synth.make_alpha_draws(steps * w.B * w.k, device="cuda")
+    return greedy, ref.cuda()
+
+
+def _injected_steps(eng, ids, w, ref, steps, alpha, seed_off=0):
+    draws = synth.make_alpha_draws(steps * w.B * w.k + seed_off, device="cuda")[seed_off:]
     offs = synth.make_wrong_offsets(steps * w.B * w.k, w.target.V, device="cuda")
     emitted = [[] for _ in range(w.B)]
     for st in range(steps):
@@ -121,6 +88,77 @@ def test_speculative_equals_greedy_on_gpu(name):
             n = int(ne[b])
             assert 1 <= n <= w.k + 1
             emitted[b] += out[b, :n].cpu().tolist()
+    return emitted
+
+
+LARGE = [n for n, w in configs.WORKLOADS.items() if not w.prompt]
+SAMPLE = {"e2b_q4_0_b4_ctx4096_k4": [1, 3], "e4b_bf16_b8_ragged_k4": [0, 5],
+          "dense30b_bf16_b8_ctx8192_k4": [6]}
+# tokens compared against the oracle's free-running greedy decode (one oracle
+# target pass per token; a ~30B-class pass takes seconds on the host cores)
+GREEDY_CMP = {"dense30b_bf16_b1_ctx8192_k4": 12, "dense30b_bf16_b8_ctx8192_k4": 12}
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_workload_matches_oracle(name):
+    w = configs.WORKLOADS[name]
+    t = w.target
+    steps_extra = (STEPS + 3) * (w.k + 1) + 64
+    tw, dw, eng, ids, ctx, kvs, first = _setup(w, steps_extra)
+    sample = SAMPLE.get(name, [0])
+    # GPU: draft, then verify the drafted rows with full logits
+    d = eng.spec_draft(ids, w.B, w.k).clone()
+    logits = torch.empty((w.B * (w.k + 1), t.V), dtype=torch.float32, device="cuda")
+    eng.sync()
+    pend = eng.pending.clone().cpu()
+    hid = eng.hid.clone().cpu()
+    out, ne = eng.spec_verify(ids, d, logits)
+    eng.sync()
+    out, ne, d = out.cpu(), ne.cpu(), d.cpu()
+    logits = logits.cpu().numpy()
+    # GPU: further speculative steps at the workload's acceptance rate
+    _, ref = _gpu_greedy_ref(eng, ids, w, STEPS * (w.k + 1) + w.k + 2)
+    more = _injected_steps(eng, ids, w, ref, STEPS, w.alphas[-1])
+    eng.close()
+    del eng
+    torch.cuda.empty_cache()
+
+    T, D = oracle.Target(tw), oracle.Drafter(dw)
+    tol = TOL[t.wdtype]
+    for b in sample:
+        s = oracle.Seq(T, ctx[b] + steps_extra)
+        s.load_prefilled(kvs[b].cpu())
+        oracle.prefill(T, s, first[b].numpy())
+        assert int(pend[b]) == s.pending
+        assert_rows_close(hid[b:b + 1].numpy(), s.hid[None], tol, "%s seq %d hidden" % (name, b))
+        ref_d, mg_d = oracle.draft(T, D, s.clone(), w.k)
+        if compare_tokens(d[b].numpy(), ref_d, mg_d) == w.k:
+            # same drafts on both sides (the oracle runs its own): verify logits and accept
+            am, mg, _, lg = oracle.forward(T, s.clone(), [s.pending] + list(ref_d), want_logits=True)
+            rows = logits[b * (w.k + 1):(b + 1) * (w.k + 1)]
+            assert_rows_close(rows, lg, tol, "%s seq %d verify logits" % (name, b))
+            em, _ = oracle.verify(T, s.clone(), ref_d)
+            n = int(ne[b])
+            compare_tokens(out[b, :n].numpy(), em, mg)
+            if np.all(mg[:len(em)] > 0.05):
+                assert n == len(em)
+        # every token the GPU emitted over all steps against the oracle's own
+        # free-running greedy decode from the same state
+        seq = out[b, :int(ne[b])].tolist() + more[b]
+        n_cmp = min(len(seq), GREEDY_CMP.get(name, len(seq)))
+        G, mgG = oracle.greedy(T, s.clone(), n_cmp)
+        compare_tokens(seq[:n_cmp], G, mgG)
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_speculative_equals_greedy_on_gpu(name):
+    """Speculative steps with drafts injected at the workload's acceptance rate
+    emit exactly the tokens of the GPU's own plain greedy decoding."""
+    w = configs.WORKLOADS[name]
+    tw, dw, eng, ids, ctx, kvs, first = _setup(w, steps_extra=(STEPS + 2) * (w.k + 1) + 64)
+    greedy, ref = _gpu_greedy_ref(eng, ids, w, STEPS * (w.k + 1) + w.k + 2)
+    alpha = w.alphas[-1] if w.alphas else 0.5
+    emitted = _injected_steps(eng, ids, w, ref, STEPS, alpha)
     for b in range(w.B):
         assert emitted[b] == greedy[b, 1:1 + len(emitted[b])].tolist(), (name, b)
     eng.close()

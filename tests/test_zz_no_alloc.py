@@ -1,13 +1,20 @@
 """spec_linear_noalloc: the projection entry point for callers that cannot
-allocate device memory (its scratch is a fixed array inside the library).
-Its results must equal spec_linear's, call after call, since every call reuses
-the same scratch. Collected last so a failure here comes after every other
+allocate device memory (a host that owns the whole device-memory budget, a
+plugin whose framework allocator must see every allocation, or code that must
+not reach cudaMalloc because it may synchronise the device). Its scratch is a
+fixed array inside the library that every call reuses, so the test checks two
+calls in a row: each against the oracle's exact fp64 linear layer at the
+kernel-level tolerance, and against spec_linear on the same inputs. Row counts
+above 8 run there as 8-row passes sharing that one array, so M = 9, 40 and 64
+are covered too. Collected last so that a failure here comes after every other
 test has run."""
 import ctypes as C
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from speculative_decoding_spec_gb300 import binding, configs, synth
 from tests.parity import assert_rows_close
 
@@ -20,24 +27,41 @@ def _x(M, K, seed):
     return torch.randn((M, K), generator=torch.Generator(device="cuda").manual_seed(seed), device="cuda")
 
 
+def _rms_gain(x, gain, eps=1e-6):
+    """The input the kernel projects, through the oracle's RMSNorm when a gain
+    is given."""
+    xd = x.double().cpu().numpy()
+    if gain is None:
+        return xd
+    g = gain.cpu().numpy()
+    return np.stack([oracle.rmsnorm(row, g, eps) for row in xd])
+
+
 @pytest.mark.parametrize("dtype,N,K,M,norm", [
-    (configs.BF16, 4112, 1536, 5, False),      # ragged N, tensor-core path with split tiles
+    (configs.BF16, 4112, 1536, 5, False),      # ragged N
     (configs.BF16, 1536, 6144, 4, True),       # long K, fused RMSNorm
     (configs.Q4_0, 1000, 1536, 3, True),
+    (configs.BF16, 1000, 1536, 9, False),      # 8-row passes: 8 + 1
+    (configs.BF16, 4112, 2048, 40, True),
+    (configs.BF16, 300, 256, 64, False),
+    (configs.Q4_0, 1000, 1536, 9, False),
+    (configs.Q4_0, 4112, 2048, 40, True),
+    (configs.Q4_0, 300, 256, 64, False),
 ])
-def test_noalloc_matches_spec_linear_on_two_calls(dtype, N, K, M, norm):
+def test_noalloc_matches_oracle_and_spec_linear_on_two_calls(dtype, N, K, M, norm):
     from speculative_decoding_spec_gb300 import build
     build.build()
     g = torch.Generator(device="cuda").manual_seed(N + K)
     w = synth.make_matrix(g, dtype, 1, N, K, 0.02, "cuda")
     gain = (torch.rand(K, generator=g, device="cuda") + 0.5) if norm else None
-    ref = binding.spec_linear(w, _x(M, K, 1), gain=gain)
     for call in range(2):
         x = _x(M, K, 1 + call)
-        ref = binding.spec_linear(w, x, gain=gain)
         y = binding.spec_linear_noalloc(w, x, gain=gain)
+        ref = binding.spec_linear(w, x, gain=gain)
         torch.cuda.synchronize()
-        assert_rows_close(y.cpu().numpy(), ref.cpu().numpy(), TOL, "noalloc call %d" % call)
+        exact = oracle.linear(w, _rms_gain(x, gain))
+        assert_rows_close(y.cpu().numpy(), exact, TOL, "noalloc call %d vs oracle" % call)
+        assert_rows_close(y.cpu().numpy(), ref.cpu().numpy(), TOL, "noalloc call %d vs spec_linear" % call)
 
 
 def test_noalloc_rejects_oversized_n():
