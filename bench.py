@@ -173,15 +173,31 @@ def greedy_reference(eng, ids, w, n_tokens):
     return ref
 
 
+WIDE_MIN_ELEMS = 1 << 25   # bf16 matrices this large (with rows of >= 4096 columns) take the
+WIDE_MIN_K = 4096          # tcgen05 projection at any row count
+
+
 def roofline_kernel_name(w):
-    """The projection kernel the verify pass of this workload runs."""
+    """The projection kernel(s) the verify pass of this workload runs, the one
+    streaming most of the bytes first."""
     t = w.target
-    if t.wdtype in (configs.BF16, configs.Q4_0) and w.M > 8:
-        return "wide_kernel (tcgen05 weight-streaming projection%s; each launch with its wide_prep_kernel)" % (
-            ", Q4_0 dequantised in shared memory" if t.wdtype == configs.Q4_0 else "")
-    if t.wdtype in (configs.BF16, configs.Q4_0):
-        return "gemv_tc_kernel (mma.sync weight-streaming projection)"
-    return "gemv_kernel (CUDA-core weight-streaming projection)"
+    if t.wdtype == configs.F32:
+        return "gemv_kernel (CUDA-core weight-streaming projection)"
+    wide = "wide_kernel (tcgen05 weight-streaming projection%s; each launch with its wide_prep_kernel)" % (
+        ", Q4_0 dequantised in shared memory" if t.wdtype == configs.Q4_0 else "")
+    if w.M > 8:
+        return wide
+    reg = "gemv_tc_kernel (mma.sync weight-streaming projection)"
+    if t.wdtype != configs.BF16:
+        return reg
+    shapes = [(t.nqkv, t.d), (t.d, t.nq * t.hd), (2 * t.ff, t.d), (t.d, t.ff)]
+    large = lambda N, K: N * K >= WIDE_MIN_ELEMS and K >= WIDE_MIN_K
+    big = sum(t.L * N * K for N, K in shapes if large(N, K)) + (t.V * t.d if large(t.V, t.d) else 0)
+    small = sum(t.L * N * K for N, K in shapes if not large(N, K)) + (0 if large(t.V, t.d) else t.V * t.d)
+    if small == 0:
+        return wide
+    return (wide + " for the large matrices, " + reg + " for the rest") if big >= small else (
+        reg + " for the per-layer matrices, " + wide + " for the large ones")
 
 
 def time_dominant_kernel(tw, w, device, reps=5):

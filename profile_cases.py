@@ -11,8 +11,8 @@ Each summary under profiles/ names the case and the ncu command it ran.
         twice. About 0.86 GB of weights.
     python profile_cases.py projections_30b
         one layer of the ~30B-class bf16 target (QKV, O, gate/up, down: 1.08
-        GB) and its LM head (3.2 GB) at M = 40 rows (batch 8, k = 4), run
-        twice: the matrix shapes of the bench's roofline kernel.
+        GB) at M = 40 rows (batch 8, k = 4), run twice: the per-layer matrix
+        shapes of the bench's roofline kernel.
     python profile_cases.py projections_30b_m5
         the same shapes at M = 5 rows (batch 1, k = 4).
     python profile_cases.py projections_wide_q4
@@ -72,10 +72,10 @@ def projections(w):
         torch.cuda.synchronize()
 
 
-def _one_layer_and_head(t, M, seed):
+def _one_layer_and_head(t, M, seed, head=True):
     g = torch.Generator(device="cuda").manual_seed(seed)
-    seq = [(synth.make_matrix(g, t.wdtype, 1, N, K, t.wstd, "cuda"), K)
-           for N, K in ((t.nqkv, t.d), (t.d, t.nq * t.hd), (2 * t.ff, t.d), (t.d, t.ff), (t.V, t.d))]
+    shapes = [(t.nqkv, t.d), (t.d, t.nq * t.hd), (2 * t.ff, t.d), (t.d, t.ff)] + ([(t.V, t.d)] if head else [])
+    seq = [(synth.make_matrix(g, t.wdtype, 1, N, K, t.wstd, "cuda"), K) for N, K in shapes]
     xs = {K: torch.randn((M, K), device="cuda") for _, K in seq}
     ys = [torch.empty((M, W.N), device="cuda") for W, _ in seq]
     for _ in range(2):
@@ -89,11 +89,11 @@ def projections_wide(w):
 
 
 def projections_30b(w):
-    _one_layer_and_head(configs.DENSE30B, 40, 5)
+    _one_layer_and_head(configs.DENSE30B, 40, 5, head=False)
 
 
 def projections_30b_m5(w):
-    _one_layer_and_head(configs.DENSE30B, 5, 5)
+    _one_layer_and_head(configs.DENSE30B, 5, 5, head=False)
 
 
 def projections_wide_q4(w):

@@ -22,13 +22,17 @@
 // memory. K and V pages arrive by TMA in the 128-byte swizzle layout: K is a
 // K-major A operand, V (stored [key][dim]) an MN-major one, the same bytes.
 //
-// Roles (one CTA per SM): warp 0 issues the TMA loads (K ring of 3 blocks, V
-// ring of 2), warp 1 the MMAs, warps 2-5 run the softmax: thread = key of the
-// block, so a column (query) maximum is a transposing warp reduction plus a
-// 4-warp combine in shared memory. The running maximum is only raised when a
-// block's maximum exceeds it by 2^8 (then O^T is rescaled in tensor memory),
-// so probabilities stay below 256 and rescales are rare. Each thread keeps
-// its own partial sums; they are reduced once per split.
+// Roles (one CTA per SM): warp 0 issues the TMA loads (K ring of 2 blocks, V
+// ring of 3: a V tile is needed a whole softmax later than the K tile of the
+// same block), warp 1 the MMAs, warps 2-9 run the softmax in two groups of
+// four (one warp per TMEM lane quarter, each group half of the query columns):
+// thread = key of the block, so a column (query) maximum is a transposing warp
+// reduction plus a 4-warp combine in shared memory. The running maximum is
+// only raised when some score exceeds it by 2^8 (one OR-reducing barrier per
+// block decides; then O^T is rescaled in tensor memory), so probabilities stay
+// below 256 and the column reductions are rare. Each thread keeps its own
+// partial sums; they are reduced once per split. The probabilities are written
+// as an MN-major operand (one 128-byte row per key, two tiles alternating).
 //
 // Work split. When the pairs are fewer than the SMs, each pair gets one CTA
 // plus a share of the others in proportion to its blocks (computed on the
@@ -59,7 +63,7 @@ constexpr int BK = 128;                       // keys per block (two pages)
 constexpr int NTHR = 320;                     // warp 0 TMA, warp 1 MMA, warps 2-9 softmax
 constexpr int SM0 = 64;                       // first softmax thread
 constexpr int NSM = 256;                      // softmax threads: 2 column groups x 4 lane quarters
-constexpr int KSLOTS = 3, VSLOTS = 2;
+constexpr int KSLOTS = 2, VSLOTS = 3;
 constexpr int HALF_BYTES = BK * 128;          // one 64-dim half of a block: 128 rows x 128 B
 constexpr int TILE_BYTES = 2 * HALF_BYTES;    // K (or V) of a block: 32 KB
 constexpr int BOX_BYTES = PAGE * 128;         // one TMA box: 64 rows x 64 dims

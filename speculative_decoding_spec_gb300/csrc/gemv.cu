@@ -473,14 +473,19 @@ void setup_gemv_attributes() {
   set_attrs_wt<DT_Q4_0>();
 }
 
-// More than 8 rows of bf16 weights with the tcgen05 scratch present: passes of
-// up to 64 rows through the tcgen05 kernel (gemm_wide.cu), each streaming the
-// weights once. Otherwise passes of at most 8 rows (each streams W again).
+// More than 8 rows of bf16 / Q4_0 weights, or a bf16 matrix of at least
+// WIDE_MIN_ELEMS elements, with the tcgen05 scratch present: passes of up to
+// 64 rows through the tcgen05 kernel (gemm_wide.cu), each streaming the
+// weights once. Otherwise passes of at most 8 rows on the register-fragment
+// kernel (each streams W again). The choice for a matrix does not depend on
+// the row count when the matrix is large, so a one-row decode and a k+1-row
+// verify of it run the same kernel.
 int gemv(const GemvArgs& a0, cudaStream_t st) {
   int launched = 0;
   GemvArgs first = a0;
   first.M = std::min(64, a0.M);
-  const bool wide = a0.M > 8 && gemv_wide_ok(first);
+  const bool large = a0.W.dtype == DT_BF16 && (long long)a0.N * a0.K >= WIDE_MIN_ELEMS && a0.K >= WIDE_MIN_K;
+  const bool wide = (a0.M > 8 || large) && gemv_wide_ok(first);
   const int step = wide ? 64 : 8;
   for (int m0 = 0; m0 < a0.M; m0 += step) {
     GemvArgs a = a0;

@@ -207,6 +207,14 @@ int gemv_tc(const GemvArgs& a, float* fix, unsigned int* cnt, cudaStream_t st);
 size_t gemv_tc_fixup_bytes();
 void setup_gemv_wide_attributes();
 bool gemv_wide_ok(const GemvArgs& a);
+// bf16 matrices of at least this many elements (64 MB) take the tcgen05 path at
+// any row count: they stream at about 70-90% of the HBM rate there, the
+// register-fragment kernel reaches about half of it on long rows.
+constexpr long long WIDE_MIN_ELEMS = 1ll << 25;
+// ... and rows of at least this many columns (shorter rows stream well on the
+// register-fragment kernel: a 262144 x 1536 LM head reaches about 88% of the
+// copy bandwidth there)
+constexpr int WIDE_MIN_K = 4096;
 int gemv_wide(const GemvArgs& a, cudaStream_t st);
 size_t gemv_wide_fix_bytes();
 // bytes of WideScratch for activation planes of up to kmax columns (0 when kmax == 0)

@@ -82,7 +82,13 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
   w.tc_fix = b.take<float>(base, gemv_tc_fixup_bytes() / sizeof(float));
   w.tc_cnt = b.take<unsigned int>(base, tc_counters(m, d));
   w.err = b.take<int>(base, 4);
-  if (M > 8) {
+  // a matrix taking the tcgen05 path at any row count (large and long rows)
+  const int qd_ = m.n_q_heads * m.head_dim;
+  const bool big = (m.d_model >= WIDE_MIN_K && ((long long)m.vocab * m.d_model >= WIDE_MIN_ELEMS ||
+                                                2ll * m.d_ff * m.d_model >= WIDE_MIN_ELEMS)) ||
+                   (qd_ >= WIDE_MIN_K && (long long)m.d_model * qd_ >= WIDE_MIN_ELEMS) ||
+                   (m.d_ff >= WIDE_MIN_K && (long long)m.d_model * m.d_ff >= WIDE_MIN_ELEMS);
+  if (M > 8 || (m.w_dtype == SPEC_BF16 && big)) {
     // widest reduction of any projection: target d, q heads, FFN; drafter input [h; e], width, heads, FFN
     int kmax = std::max({2 * m.d_model, m.n_q_heads * m.head_dim, m.d_ff});
     if (d) kmax = std::max({kmax, d->hidden, d->n_q_heads * m.head_dim, d->d_ff});
@@ -421,8 +427,8 @@ int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st) {
   g.wide = c->wk.wide;
   if (c->wtrace && c->wtrace_n < WTRACE_LAUNCHES) {
     unsigned long long* slot = c->wtrace + (size_t)(c->wtrace_n++) * num_sms() * 16;
-    if (g.M > 8) g.wide.trace = slot;
-    else g.tc_trace = slot;
+    g.wide.trace = slot;  // whichever projection kernel runs records into the slot
+    g.tc_trace = slot;
   }
   g.prefetch = c->prefetch ? 1 : 0;
   return gemv(g, st);
@@ -613,7 +619,8 @@ spec_status spec_inject_drafts(spec_ctx* c, int32_t B, const int32_t* seq_ids, i
 size_t spec_linear_workspace_bytes(int32_t N, int32_t K, int32_t M) {
   if (N <= 0 || K <= 0 || M <= 0) return 0;
   size_t n = gemv_tc_fixup_bytes() + (((size_t)N / 8 + 64) * sizeof(unsigned int) + 255) / 256 * 256 + 256;
-  if (M > 8) n += gemv_wide_fix_bytes() + gemv_wide_xs_bytes(K) + 64 * sizeof(float) + 3 * 256;
+  if (M > 8 || ((long long)N * K >= WIDE_MIN_ELEMS && K >= WIDE_MIN_K))
+    n += gemv_wide_fix_bytes() + gemv_wide_xs_bytes(K) + 64 * sizeof(float) + 3 * 256;
   return n;
 }
 
@@ -626,7 +633,7 @@ spec_status spec_linear(const spec_matrix* w, int32_t N, int32_t K, const float*
   g.epi = EPI_STORE; g.Y = y; g.ldy = N; g.pdl = 0; g.prefetch = 0;
   g.tc_fix = (float*)workspace;
   g.tc_cnt = (unsigned int*)((char*)workspace + gemv_tc_fixup_bytes());
-  if (M > 8) {
+  if (M > 8 || ((long long)N * K >= WIDE_MIN_ELEMS && K >= WIDE_MIN_K)) {
     char* p = (char*)workspace + gemv_tc_fixup_bytes() +
               (((size_t)N / 8 + 64) * sizeof(unsigned int) + 255) / 256 * 256 + 256;
     g.wide.fix = (float*)p;
