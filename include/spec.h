@@ -151,10 +151,12 @@ typedef struct {
 
 typedef struct spec_ctx spec_ctx;
 
-/* Bytes of workspace needed for batches of up to B_max sequences, up to
- * rows_max rows per sequence per pass (>= k_max + 1, and >= the longest
- * prompt given to spec_prefill) and sequences of up to max_pages_per_seq KV
- * pages. Returns 0 on invalid descriptors. */
+/* Bytes of workspace needed for batches of up to B_max sequences, prompts of
+ * up to rows_max tokens per sequence (>= k_max + 1) and sequences of up to
+ * max_pages_per_seq KV pages. A target pass takes at most
+ * P = min(rows_max, 64, 128 / (n_q_heads / n_kv_heads)) rows per sequence;
+ * longer prompts run as consecutive passes of P rows, and k_max + 1 <= P.
+ * Returns 0 on invalid descriptors. */
 size_t spec_workspace_bytes(const spec_model_desc *m, const spec_drafter_desc *d,
                             int32_t B_max, int32_t rows_max, int32_t max_pages_per_seq);
 
@@ -171,9 +173,14 @@ spec_status spec_init(const spec_model_desc *model, const spec_weights *weights,
 
 /* Prompt processing: feed R tokens per sequence (tokens "device" int32 [B][R])
  * at positions seq_len..seq_len+R-1, commit them all, set pending to the
- * target's choice after the last one and hid to its hidden state. seq_ids
- * ("device" int32 [B]) name distinct slots. A caller that filled the cache
- * itself sets seq_len first and feeds the last prompt token with R = 1. */
+ * target's choice after the last one and hid to its hidden state. The target
+ * processes the whole context before drafting starts; the drafter has no
+ * prefill of its own ("Accelerating Gemini Nano on Pixel with frozen
+ * multi-token prediction" (ai-news-spoon), section "Zero-copy architecture").
+ * R <= rows_max; prompts longer than a pass (see spec_workspace_bytes) run as
+ * consecutive causal passes within the call. seq_ids ("device" int32 [B])
+ * name distinct slots. A caller that filled the cache itself sets seq_len
+ * first and feeds the last prompt token with R = 1. */
 spec_status spec_prefill(spec_ctx *ctx, int32_t B, const int32_t *seq_ids, int32_t R,
                          const int32_t *tokens, void *stream);
 
@@ -186,10 +193,26 @@ spec_status spec_draft(spec_ctx *ctx, int32_t B, const int32_t *seq_ids, int32_t
  * accept, KV-length rollback. out_tokens ("device" int32 [B][k+1]) gets the
  * emitted tokens t_0..t_A followed by -1; n_emitted ("device" int32 [B]) gets
  * A+1 in [1, k+1]. logits_dbg ("device" float [B*(k+1)][vocab]) may be NULL;
- * when given it receives every row's logits. k in [0, rows_max-1]. */
+ * when given it receives every row's logits. k in [0, P-1], P the rows of a
+ * pass (see spec_workspace_bytes). */
 spec_status spec_verify(spec_ctx *ctx, int32_t B, const int32_t *seq_ids, int32_t k,
                         const int32_t *drafts, int32_t *out_tokens, int32_t *n_emitted,
                         float *logits_dbg, void *stream);
+
+/* Lenient verify ("Accelerating Gemini Nano on Pixel with frozen multi-token
+ * prediction" (ai-news-spoon), section "Future directions": relaxing the strict
+ * token match between draft and verification for some uses; the pages give no
+ * rule). Here draft d_j is accepted while every earlier draft was and d_j ranks
+ * among the target's top_m tokens of row j-1 (rank = tokens with a higher
+ * binary32 logit, or an equal one and a lower index); the step emits the
+ * accepted drafts followed by the target's own choice at the next row, commits
+ * those rows and rolls the rest back, as spec_verify does. top_m = 1 is
+ * spec_verify's greedy accept; larger values no longer reproduce plain greedy
+ * decoding. k in [1, P-1] (P as for spec_verify), top_m >= 1. The rows' logits go to
+ * logits_dbg when given, else to the workspace. */
+spec_status spec_verify_topm(spec_ctx *ctx, int32_t B, const int32_t *seq_ids, int32_t k,
+                             const int32_t *drafts, int32_t top_m, int32_t *out_tokens,
+                             int32_t *n_emitted, float *logits_dbg, void *stream);
 
 /* spec_draft followed by spec_verify on the context's own draft buffer. */
 spec_status spec_step(spec_ctx *ctx, int32_t B, const int32_t *seq_ids, int32_t k,

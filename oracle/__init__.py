@@ -45,6 +45,9 @@ def lib():
         _lib.or_accept.restype = i
         _lib.or_accept.argtypes = [i, p, p]
         _lib.or_verify.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), i, p, p, p, p]
+        _lib.or_rank_f32.restype = i
+        _lib.or_rank_f32.argtypes = [p, i, i]
+        _lib.or_verify_topm.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), i, p, i, p, p, p, p]
         _lib.or_greedy.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), i, p, p]
         _lib.or_draft.argtypes = [C.POINTER(OrModel), C.POINTER(OrDrafter), C.POINTER(OrSeq), i,
                                   p, p]
@@ -237,6 +240,25 @@ def verify(t: Target, s: Seq, drafts):
                          _ptr(ne), _ptr(mg))
     assert rc == 0
     return out[: ne[0]].copy(), mg
+
+
+def verify_topm(t: Target, s: Seq, drafts, top_m: int):
+    """Lenient verify step. Returns (emitted tokens, margins[k+1], decision[k])."""
+    d = _i32(drafts)
+    k = d.shape[0]
+    out = np.zeros(k + 1, np.int32)
+    ne = np.zeros(1, np.int32)
+    mg = np.zeros(k + 1, np.float64)
+    dec = np.zeros(max(k, 1), np.float64)
+    rc = lib().or_verify_topm(C.byref(t.m), C.byref(s.c), k, _ptr(d) if k else None, top_m, _ptr(out),
+                              _ptr(ne), _ptr(mg), _ptr(dec))
+    assert rc == 0
+    return out[: ne[0]].copy(), mg, dec[:k]
+
+
+def rank_f32(logits, tok: int) -> int:
+    lg = np.ascontiguousarray(np.asarray(logits, np.float64))
+    return lib().or_rank_f32(_ptr(lg), lg.shape[0], tok)
 
 
 def greedy(t: Target, s: Seq, n: int):

@@ -384,6 +384,89 @@ int or_verify(const or_model *m, or_seq *s, int k, const int32_t *drafts,
     return rc;
 }
 
+/* Rank of token `tok` among n binary32-rounded logits: the number of tokens
+ * ordered before it (a higher logit, or the same logit and a lower index). */
+int or_rank_f32(const double *logits, int n, int tok)
+{
+    float ft = (float)logits[tok];
+    int r = 0;
+    for (int i = 0; i < n; ++i) {
+        float f = (float)logits[i];
+        if (f > ft || (f == ft && i < tok))
+            ++r;
+    }
+    return r;
+}
+
+/* Lenient verify ([P4 "Future directions"]: the strict token match between
+ * draft and verification is relaxed for some uses; the pages give no rule).
+ * Reading: draft d_j is accepted while it ranks among the target's top_m
+ * tokens of row j-1 (or_rank_f32 < top_m), every earlier draft having been
+ * accepted; the step emits the accepted drafts followed by the target's own
+ * choice t_A at row A, and keeps rows 0..A in the cache. top_m = 1 is the
+ * greedy accept of or_verify. decision (optional, [k]) receives, per draft,
+ * the logit distance between the draft and the rank boundary it was judged
+ * against (how far the accept decision is from flipping); margins [k+1] the
+ * rows' top-1 minus top-2 gaps. */
+int or_verify_topm(const or_model *m, or_seq *s, int k, const int32_t *drafts, int top_m,
+                   int32_t *out_tokens, int32_t *n_emitted, double *margins, double *decision)
+{
+    int R = k + 1;
+    int32_t *rows = (int32_t *)malloc(sizeof(int32_t) * (size_t)R);
+    int32_t *t = (int32_t *)malloc(sizeof(int32_t) * (size_t)R);
+    double *hid = (double *)malloc(sizeof(double) * (size_t)R * m->d);
+    double *lg = (double *)malloc(sizeof(double) * (size_t)R * m->V);
+    float *sorted = (float *)malloc(sizeof(float) * (size_t)m->V);
+    rows[0] = s->pending;
+    for (int j = 0; j < k; ++j)
+        rows[j + 1] = drafts[j];
+    int rc = or_forward(m, s, rows, R, lg, t, margins, hid);
+    if (rc == 0) {
+        int A = 0;
+        for (int j = 0; j < k; ++j) {
+            const double *row = lg + (int64_t)j * m->V;
+            int d = drafts[j];
+            int ok = d >= 0 && d < m->V && or_rank_f32(row, m->V, d) < top_m;
+            if (decision) {
+                /* the top_m-th and (top_m+1)-th largest binary32 logits */
+                for (int i = 0; i < m->V; ++i)
+                    sorted[i] = (float)row[i];
+                double inside = -INFINITY, outside = -INFINITY;
+                for (int r = 0; r <= top_m && r < m->V; ++r) {
+                    int best = -1;
+                    for (int i = 0; i < m->V; ++i)
+                        if (sorted[i] != -INFINITY && (best < 0 || sorted[i] > sorted[best]))
+                            best = i;
+                    if (best < 0)
+                        break;
+                    if (r == top_m - 1)
+                        inside = sorted[best];
+                    if (r == top_m)
+                        outside = sorted[best];
+                    sorted[best] = -INFINITY;
+                }
+                double fd = d >= 0 && d < m->V ? (double)(float)row[d] : -INFINITY;
+                decision[j] = ok ? fd - outside : inside - fd;
+            }
+            if (!ok)
+                break;
+            ++A;
+        }
+        if (decision)
+            for (int j = A + 1; j < k; ++j)
+                decision[j] = INFINITY;  /* never judged */
+        for (int j = 0; j < A; ++j)
+            out_tokens[j] = drafts[j];
+        out_tokens[A] = t[A];
+        *n_emitted = A + 1;
+        s->len += A + 1;
+        s->pending = t[A];
+        memcpy(s->hid, hid + (int64_t)A * m->d, sizeof(double) * m->d);
+    }
+    free(rows); free(t); free(hid); free(lg); free(sorted);
+    return rc;
+}
+
 /* Plain greedy decoding: one token per target pass. */
 int or_greedy(const or_model *m, or_seq *s, int n, int32_t *out, double *margins)
 {

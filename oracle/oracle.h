@@ -126,6 +126,16 @@ int or_accept(int k, const int32_t *drafts, const int32_t *t);
 /* One verify step: rows [pending, drafts], accept, emit, roll back. */
 int or_verify(const or_model *m, or_seq *s, int k, const int32_t *drafts,
               int32_t *out_tokens, int32_t *n_emitted, double *margins);
+/* Rank of token tok among n logits rounded to binary32: how many tokens come
+ * before it (higher logit, or equal logit and lower index). */
+int or_rank_f32(const double *logits, int n, int tok);
+/* Lenient verify: accept drafts while each ranks among the target's top_m
+ * tokens at its row; emit the accepted drafts then the target's own choice.
+ * top_m = 1 is or_verify. decision [k] (optional): per draft, the logit
+ * distance to the rank boundary it was judged against (INFINITY if not
+ * judged). */
+int or_verify_topm(const or_model *m, or_seq *s, int k, const int32_t *drafts, int top_m,
+                   int32_t *out_tokens, int32_t *n_emitted, double *margins, double *decision);
 /* n plain greedy steps (verify with k = 0); out[i] = emitted token i. */
 int or_greedy(const or_model *m, or_seq *s, int n, int32_t *out, double *margins);
 

@@ -53,7 +53,7 @@ __global__ void embed_rows_kernel(RowsArgs a) {
   const int m = blockIdx.x, b = m / a.R, i = m % a.R;
   const int slot = a.seq_ids[b];
   int tok;
-  if (a.mode == TAIL_PREFILL) tok = a.tokens[b * a.R + i];
+  if (a.mode == TAIL_PREFILL) tok = a.tokens[(size_t)b * a.tok_ld + i];
   else tok = i == 0 ? a.pending[slot] : a.tokens[b * (a.R - 1) + i - 1];
   if (tok < 0 || tok >= a.vocab) {
     if (threadIdx.x == 0) set_error(a.err, SPEC_ERR_TOKEN);

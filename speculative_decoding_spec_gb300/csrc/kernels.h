@@ -107,7 +107,8 @@ int gemv(const GemvArgs& a, cudaStream_t st);
 struct RowsArgs {
   int B, R, mode;           // mode: TAIL_VERIFY (rows = [pending, drafts]) or TAIL_PREFILL
   const int32_t* seq_ids;
-  const int32_t* tokens;    // PREFILL: [B][R]; VERIFY: drafts [B][R-1]
+  const int32_t* tokens;    // PREFILL: [B][tok_ld], this pass's R from column 0; VERIFY: drafts [B][R-1]
+  int tok_ld;               // PREFILL: row stride of tokens (the whole prompt's length)
   const int32_t* pending;
   const int32_t* seq_len;
   Mat embed;
@@ -156,6 +157,23 @@ struct AttnArgs {
   int* err;
 };
 int attention(const AttnArgs& a, cudaStream_t st);
+
+// Lenient accept (accept_topm.cu): drafts kept while each ranks among the
+// target's top_m tokens of its row; the pass's LM head wrote every row's logits
+// and its packed argmax (best, consumed and zeroed here).
+struct TopmArgs {
+  int B, k, top_m, V, S;       // S: vocabulary parts per draft (set by the launcher)
+  const int32_t* seq_ids;      // [B]
+  const int32_t* drafts;       // [B][k]
+  const float* logits;         // [B*(k+1)][V]
+  unsigned long long* best;    // [B*(k+1)]
+  unsigned int* rank;          // [B*k] counts, zero between launches
+  unsigned int* counter;       // arrival counter, zero between launches
+  int32_t *out_tokens, *n_emitted, *seq_len, *pending, *sel_row;
+  int64_t* stats;
+  int* err;
+};
+int topm_accept(const TopmArgs& a, cudaStream_t st);
 
 // Final-normed hidden state of the row chosen by the accept step -> slot state.
 // Skipped when the device error word `err` is set (the pass commits nothing).

@@ -35,6 +35,8 @@ struct Work {
   unsigned long long* best;
   unsigned int* counter;
   unsigned int* attn_count;
+  float* lg;                // [M][V] row logits (lenient accept)
+  unsigned int *rank, *rank_cnt;
   float* tc_fix;
   unsigned int* tc_cnt;
   WideScratch wide;         // tcgen05 projection scratch (null when passes have <= 8 rows)
@@ -60,11 +62,19 @@ size_t tc_counters(const spec_model_desc& m, const spec_drafter_desc* d) {
   return n / 8 + 64;
 }
 
+// Rows of one target pass per sequence: at most 64, and at most 128 query rows
+// (rows x GQA group) per (sequence, KV head) for the attention. A longer
+// prompt runs as consecutive passes of this many rows.
+int pass_rows(const spec_model_desc& m, int rows_max) {
+  const int G = m.n_q_heads / m.n_kv_heads;
+  return std::max(1, std::min({rows_max, 64, 128 / G}));
+}
+
 Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int B_max, int rows_max,
            int max_pages) {
   Work w = {};
   Buf b;
-  const size_t M = (size_t)B_max * rows_max;
+  const size_t M = (size_t)B_max * pass_rows(m, rows_max);
   const int nqkv = (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim, qd = m.n_q_heads * m.head_dim;
   w.x = b.take<float>(base, M * m.d_model);
   w.qkv = b.take<float>(base, M * nqkv);
@@ -79,6 +89,9 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
   w.best = b.take<unsigned long long>(base, M);
   w.counter = b.take<unsigned int>(base, 4);
   w.attn_count = b.take<unsigned int>(base, (size_t)2 * B_max * m.n_kv_heads);
+  w.lg = b.take<float>(base, M * m.vocab);
+  w.rank = b.take<unsigned int>(base, (size_t)B_max * KMAX);
+  w.rank_cnt = b.take<unsigned int>(base, 4);
   w.tc_fix = b.take<float>(base, gemv_tc_fixup_bytes() / sizeof(float));
   w.tc_cnt = b.take<unsigned int>(base, tc_counters(m, d));
   w.err = b.take<int>(base, 4);
@@ -158,7 +171,7 @@ struct spec_ctx {
   spec_drafter_weights dw;
   spec_kv_desc kv;
   spec_state state;
-  int B_max, rows_max;
+  int B_max, rows_max, pass_rows;
   long long layer_elems;
   Work wk;
   bool graphs = true;
@@ -243,7 +256,8 @@ AttnWork carve_attention(char* base, int B, int R, int nq, int nkv, int hd, int 
 
 // ---- the target pass: rows -> layers -> LM head + argmax + accept -----------
 int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, const int32_t* tokens,
-                 int32_t* out_tokens, int32_t* n_emitted, float* logits, cudaStream_t st) {
+                 int32_t* out_tokens, int32_t* n_emitted, float* logits, cudaStream_t st, int top_m = 0,
+                 int tok_ld = 0) {
   const spec_model_desc& m = c->m;
   const Work& w = c->wk;
   const int M = B * R, d = m.d_model, hd = m.head_dim, nq = m.n_q_heads, nkv = m.n_kv_heads;
@@ -260,7 +274,7 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
   ra.B = B; ra.R = R; ra.mode = mode; ra.seq_ids = seq_ids; ra.tokens = tokens;
   ra.pending = c->state.pending; ra.seq_len = c->state.seq_len; ra.embed = M_(c->w.embed);
   ra.d = d; ra.hd = hd; ra.theta = m.rope_theta; ra.x = w.x; ra.pos = w.pos; ra.rope_cs = w.rope_cs;
-  ra.err = w.err; ra.vocab = m.vocab;
+  ra.err = w.err; ra.vocab = m.vocab; ra.tok_ld = tok_ld > 0 ? tok_ld : R;
   LAUNCH(embed_rows(ra, st));
 
   const bool fused_rope = c->fused_rope;
@@ -327,7 +341,20 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
   t.out_tokens = out_tokens; t.n_emitted = n_emitted; t.seq_len = c->state.seq_len;
   t.pending = c->state.pending; t.stats = c->state.stats; t.sel_row = w.sel_row;
   t.best_all = w.best; t.counter = w.counter; t.err = w.err;
+  if (top_m > 0) {
+    // lenient accept: every row's logits kept, the accept runs in its own kernel
+    if (!g.Y) g.Y = w.lg;
+    t.mode = TAIL_NONE;
+  }
   LAUNCH(run_gemv(c, g, st));
+  if (top_m > 0) {
+    TopmArgs ta = {};
+    ta.B = B; ta.k = R - 1; ta.top_m = top_m; ta.V = m.vocab; ta.seq_ids = seq_ids; ta.drafts = tokens;
+    ta.logits = g.Y; ta.best = w.best; ta.rank = w.rank; ta.counter = w.rank_cnt; ta.out_tokens = out_tokens;
+    ta.n_emitted = n_emitted; ta.seq_len = c->state.seq_len; ta.pending = c->state.pending; ta.sel_row = w.sel_row;
+    ta.stats = c->state.stats; ta.err = w.err;
+    LAUNCH(topm_accept(ta, st));
+  }
   LAUNCH(commit_hidden(B, seq_ids, w.sel_row, w.x, d, c->w.g_final, m.rms_eps, c->state.hid, w.err, st));
   return n;
 }
@@ -499,7 +526,7 @@ spec_status spec_init(const spec_model_desc* model, const spec_weights* weights,
   *out = nullptr;
   const spec_model_desc& m = *model;
   if (!model_ok(m)) return SPEC_EINVAL;
-  if (B_max <= 0 || rows_max <= 0 || rows_max > 64) return SPEC_EINVAL;
+  if (B_max <= 0 || rows_max <= 0) return SPEC_EINVAL;
   if (kv->page_size != 64 || !kv->pool || !kv->block_table || kv->n_pages <= 0 || kv->max_pages_per_seq <= 0 ||
       kv->n_slots < B_max)
     return SPEC_EINVAL;
@@ -513,7 +540,7 @@ spec_status spec_init(const spec_model_desc* model, const spec_weights* weights,
     if (mm->dtype != m.w_dtype) return SPEC_EINVAL;
   (void)nqkv;
   const int G = m.n_q_heads / m.n_kv_heads;
-  if (attention_smem(m.head_dim, rows_max * G) > 200 * 1024 || rows_max * G > 128) return SPEC_EUNSUPPORTED;
+  if (G > 128 || attention_smem(m.head_dim, pass_rows(m, rows_max) * G) > 200 * 1024) return SPEC_EUNSUPPORTED;
   if (drafter) {
     if (!dweights || !drafter_ok(m, *drafter)) return SPEC_EINVAL;
     const spec_drafter_weights& dw = *dweights;
@@ -540,6 +567,7 @@ spec_status spec_init(const spec_model_desc* model, const spec_weights* weights,
   c->state = *state;
   c->B_max = B_max;
   c->rows_max = rows_max;
+  c->pass_rows = pass_rows(m, rows_max);
   c->layer_elems = (long long)kv->n_pages * 2 * m.n_kv_heads * 64 * m.head_dim;
   c->wk = carve((char*)workspace, m, drafter, B_max, rows_max, kv->max_pages_per_seq);
   setup_device_attributes();
@@ -561,15 +589,25 @@ spec_status spec_prefill(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t
                          void* stream) {
   if (!batch_ok(c, B, seq_ids) || R <= 0 || R > c->rows_max || !tokens) return SPEC_EINVAL;
   cudaStream_t st = (cudaStream_t)stream;
+  // passes of at most pass_rows rows; each commits its rows, so the next one's
+  // rows attend to them as cached keys
   return run_graph(c, key_of("prefill", {B, R, (long long)seq_ids, (long long)tokens, (long long)st}), st,
                    [&](cudaStream_t s) {
-                     return enqueue_pass(c, B, seq_ids, R, TAIL_PREFILL, tokens, nullptr, nullptr, nullptr, s);
+                     int n = 0;
+                     for (int r0 = 0; r0 < R; r0 += c->pass_rows) {
+                       const int r = std::min(c->pass_rows, R - r0);
+                       const int k = enqueue_pass(c, B, seq_ids, r, TAIL_PREFILL, tokens + r0, nullptr, nullptr,
+                                                  nullptr, s, 0, R);
+                       if (k < 0) return -1;
+                       n += k;
+                     }
+                     return n;
                    });
 }
 
 spec_status spec_verify(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t k, const int32_t* drafts,
                         int32_t* out_tokens, int32_t* n_emitted, float* logits_dbg, void* stream) {
-  if (!batch_ok(c, B, seq_ids) || k < 0 || k > KMAX || k + 1 > c->rows_max || !out_tokens || !n_emitted ||
+  if (!batch_ok(c, B, seq_ids) || k < 0 || k > KMAX || k + 1 > c->pass_rows || !out_tokens || !n_emitted ||
       (k > 0 && !drafts))
     return SPEC_EINVAL;
   cudaStream_t st = (cudaStream_t)stream;
@@ -579,6 +617,22 @@ spec_status spec_verify(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t 
                    st, [&](cudaStream_t s) {
                      return enqueue_pass(c, B, seq_ids, k + 1, TAIL_VERIFY, drafts, out_tokens, n_emitted,
                                          logits_dbg, s);
+                   });
+}
+
+spec_status spec_verify_topm(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t k, const int32_t* drafts,
+                             int32_t top_m, int32_t* out_tokens, int32_t* n_emitted, float* logits_dbg,
+                             void* stream) {
+  if (!batch_ok(c, B, seq_ids) || k < 1 || k > KMAX || k + 1 > c->pass_rows || !out_tokens || !n_emitted ||
+      !drafts || top_m < 1)
+    return SPEC_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  return run_graph(c,
+                   key_of("verify_topm", {B, k, top_m, (long long)seq_ids, (long long)drafts, (long long)out_tokens,
+                                          (long long)n_emitted, (long long)logits_dbg, (long long)st}),
+                   st, [&](cudaStream_t s) {
+                     return enqueue_pass(c, B, seq_ids, k + 1, TAIL_VERIFY, drafts, out_tokens, n_emitted,
+                                         logits_dbg, s, top_m);
                    });
 }
 
