@@ -214,6 +214,25 @@ spec_status spec_verify_topm(spec_ctx *ctx, int32_t B, const int32_t *seq_ids, i
                              const int32_t *drafts, int32_t top_m, int32_t *out_tokens,
                              int32_t *n_emitted, float *logits_dbg, void *stream);
 
+/* Tree verify ("Accelerating Gemini Nano on Pixel with frozen multi-token
+ * prediction" (ai-news-spoon), section "Future directions": exploring branching
+ * possibilities in parallel so that long sequences are accepted more often;
+ * the pages give no algorithm). Per sequence, n draft nodes: tokens ("device"
+ * int32 [B][n]) and parents ("device" int32 [B][n]; -1: a child of the pending
+ * token, the root; else an earlier node index). One target pass verifies the
+ * root and every node: node i sits at position seq_len + depth(i) and sees the
+ * committed keys, the root and its own ancestors. Greedy accept walks from the
+ * root: the lowest-index child whose token equals the target's choice at the
+ * current node is accepted, and so on. out_tokens ([B][n+1]) gets the accepted
+ * tokens followed by the target's choice at the last accepted node, then -1;
+ * n_emitted in [1, depth + 1]. The root and the accepted nodes stay in the
+ * cache at consecutive positions (their keys and values are moved there), the
+ * other nodes are dropped. A chain (parents[i] = i - 1) is spec_verify.
+ * n in [1, P-1] (P as for spec_verify), at most 16. */
+spec_status spec_verify_tree(spec_ctx *ctx, int32_t B, const int32_t *seq_ids, int32_t n,
+                             const int32_t *tokens, const int32_t *parents, int32_t *out_tokens,
+                             int32_t *n_emitted, float *logits_dbg, void *stream);
+
 /* spec_draft followed by spec_verify on the context's own draft buffer. */
 spec_status spec_step(spec_ctx *ctx, int32_t B, const int32_t *seq_ids, int32_t k,
                       int32_t *out_tokens, int32_t *n_emitted, void *stream);

@@ -48,6 +48,7 @@ def lib():
         _lib.or_rank_f32.restype = i
         _lib.or_rank_f32.argtypes = [p, i, i]
         _lib.or_verify_topm.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), i, p, i, p, p, p, p]
+        _lib.or_verify_tree.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), i, p, p, p, p, p]
         _lib.or_greedy.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), i, p, p]
         _lib.or_draft.argtypes = [C.POINTER(OrModel), C.POINTER(OrDrafter), C.POINTER(OrSeq), i,
                                   p, p]
@@ -254,6 +255,18 @@ def verify_topm(t: Target, s: Seq, drafts, top_m: int):
                               _ptr(ne), _ptr(mg), _ptr(dec))
     assert rc == 0
     return out[: ne[0]].copy(), mg, dec[:k]
+
+
+def verify_tree(t: Target, s: Seq, tokens, parents):
+    """Tree verify step. Returns (emitted tokens, margins[n+1]: per node, root first)."""
+    tk, pa = _i32(tokens), _i32(parents)
+    n = tk.shape[0]
+    out = np.zeros(n + 1, np.int32)
+    ne = np.zeros(1, np.int32)
+    mg = np.zeros(n + 1, np.float64)
+    rc = lib().or_verify_tree(C.byref(t.m), C.byref(s.c), n, _ptr(tk), _ptr(pa), _ptr(out), _ptr(ne), _ptr(mg))
+    assert rc == 0, "or_verify_tree failed (bad parents or capacity)"
+    return out[: ne[0]].copy(), mg
 
 
 def rank_f32(logits, tok: int) -> int:

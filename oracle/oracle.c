@@ -467,6 +467,89 @@ int or_verify_topm(const or_model *m, or_seq *s, int k, const int32_t *drafts, i
     return rc;
 }
 
+/* Tree verify ([P4 "Future directions"]: exploring branching possibilities
+ * in parallel to raise the chance of accepting a long sequence; the pages give
+ * no algorithm). Reading: n draft nodes with tokens[i] and parents[i] (-1: a
+ * child of the pending token, the root; else an earlier node). The target's
+ * choice at a node is its greedy token after the root path to that node (the
+ * committed context, the pending token, the ancestors' tokens, the node's
+ * token); here each node's choice comes from a forward pass over exactly that
+ * path. Greedy accept walks from the root: the lowest-index child whose token
+ * equals the target's choice at the current node is accepted, and so on; the
+ * step emits the accepted tokens followed by the target's choice at the last
+ * accepted node, and the cache keeps the root and the accepted path at
+ * consecutive positions. A chain (parents[i] = i - 1) is or_verify. */
+int or_verify_tree(const or_model *m, or_seq *s, int n, const int32_t *tokens, const int32_t *parents,
+                   int32_t *out_tokens, int32_t *n_emitted, double *margins)
+{
+    int32_t *choice = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n + 1));
+    double *mg = (double *)malloc(sizeof(double) * (size_t)(n + 1));
+    int32_t *path = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n + 2));
+    int32_t *am = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n + 2));
+    double *mm = (double *)malloc(sizeof(double) * (size_t)(n + 2));
+    double *hid = (double *)malloc(sizeof(double) * (size_t)(n + 2) * m->d);
+    or_seq tmp = *s;
+    float *kv_save = NULL;
+    int rc = 0;
+    /* node r (r = 0: the root; r = i + 1: draft node i): its root path */
+    for (int r = 0; r <= n && rc == 0; ++r) {
+        int len = 0;
+        for (int x = r - 1; x >= 0; x = parents[x]) {
+            if (parents[x] >= x) {
+                rc = -1;
+                break;
+            }
+            path[len++] = tokens[x];
+        }
+        if (rc)
+            break;
+        path[len++] = s->pending;
+        for (int i = 0; i < len / 2; ++i) { /* root first */
+            int t = path[i];
+            path[i] = path[len - 1 - i];
+            path[len - 1 - i] = t;
+        }
+        tmp.len = s->len;
+        rc = or_forward(m, &tmp, path, len, NULL, am, mm, NULL);
+        choice[r] = am[len - 1];
+        mg[r] = mm[len - 1];
+    }
+    if (rc == 0) {
+        /* walk the tree from the root */
+        int cur = 0, A = 0;
+        for (;;) {
+            int next = -1;
+            for (int i = 0; i < n; ++i)
+                if (parents[i] + 1 == cur && tokens[i] == choice[cur]) {
+                    next = i + 1;
+                    break;
+                }
+            if (next < 0)
+                break;
+            out_tokens[A++] = tokens[next - 1];
+            cur = next;
+        }
+        out_tokens[A] = choice[cur];
+        *n_emitted = A + 1;
+        if (margins)
+            for (int r = 0; r <= n; ++r)
+                margins[r] = mg[r];
+        /* the committed rows: the root and the accepted path, written again by
+         * one forward over them at their final positions */
+        path[0] = s->pending;
+        for (int j = 0; j < A; ++j)
+            path[j + 1] = out_tokens[j];
+        rc = or_forward(m, s, path, A + 1, NULL, am, mm, hid);
+        if (rc == 0) {
+            s->len += A + 1;
+            s->pending = choice[cur];
+            memcpy(s->hid, hid + (int64_t)A * m->d, sizeof(double) * m->d);
+        }
+    }
+    free(choice); free(mg); free(path); free(am); free(mm); free(hid); free(kv_save);
+    return rc;
+}
+
 /* Plain greedy decoding: one token per target pass. */
 int or_greedy(const or_model *m, or_seq *s, int n, int32_t *out, double *margins)
 {

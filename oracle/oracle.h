@@ -136,6 +136,14 @@ int or_rank_f32(const double *logits, int n, int tok);
  * judged). */
 int or_verify_topm(const or_model *m, or_seq *s, int k, const int32_t *drafts, int top_m,
                    int32_t *out_tokens, int32_t *n_emitted, double *margins, double *decision);
+/* Tree verify: n draft nodes (tokens, parents: -1 = child of the pending
+ * token, else an earlier node); each node's target choice after its root
+ * path; accept the lowest-index matching child from the root down; emit the
+ * accepted tokens then the target's choice at the last accepted node; keep the
+ * root and the accepted path in the cache. margins [n+1]: per node (root
+ * first) the top-1 minus top-2 gap of its choice. */
+int or_verify_tree(const or_model *m, or_seq *s, int n, const int32_t *tokens, const int32_t *parents,
+                   int32_t *out_tokens, int32_t *n_emitted, double *margins);
 /* n plain greedy steps (verify with k = 0); out[i] = emitted token i. */
 int or_greedy(const or_model *m, or_seq *s, int n, int32_t *out, double *margins);
 

@@ -23,7 +23,7 @@ EXPORTS = ["spec_workspace_bytes", "spec_init", "spec_prefill", "spec_draft", "s
            "spec_decode", "spec_inject_drafts", "spec_stats", "spec_sync", "spec_set_graphs",
            "spec_kernel_launches", "spec_status_str", "spec_destroy", "spec_linear",
            "spec_linear_workspace_bytes", "spec_linear_noalloc", "spec_set_option",
-           "spec_attention_workspace_bytes", "spec_attention", "spec_verify_topm"]
+           "spec_attention_workspace_bytes", "spec_attention", "spec_verify_topm", "spec_verify_tree"]
 SPEC_OPT_GRAPHS, SPEC_OPT_PREFETCH, SPEC_OPT_TEST_ATTN_WAIT = 1, 4, 8
 SPEC_OPT_WIDE_TRACE = 7
 SPEC_LINEAR_NOALLOC_MAX_ROWS = 523776
@@ -126,6 +126,8 @@ def lib():
     L.spec_attention.argtypes = [p, p, i32, i32, p, p, i32, i32, i32, p, p, p, C.c_size_t, p]
     L.spec_verify_topm.restype = st
     L.spec_verify_topm.argtypes = [p, i32, p, i32, p, i32, p, p, p, p]
+    L.spec_verify_tree.restype = st
+    L.spec_verify_tree.argtypes = [p, i32, p, i32, p, p, p, p, p, p]
     L.spec_destroy.restype = None
     L.spec_destroy.argtypes = [p]
     _lib = L
@@ -340,6 +342,17 @@ class Engine:
         out = self._buf("out_tokens", (B, k + 1))
         ne = self._buf("n_emitted", (B,))
         check("spec_verify_topm", lib().spec_verify_topm(self.ctx, B, _ptr(seq_ids), k, _ptr(drafts), int(top_m),
+                                                         _ptr(out), _ptr(ne), _ptr(logits), self.stream.cuda_stream))
+        self.leave()
+        return out, ne
+
+    def spec_verify_tree(self, seq_ids, tokens: torch.Tensor, parents: torch.Tensor,
+                         logits: Optional[torch.Tensor] = None):
+        self.enter()
+        B, n = tokens.shape
+        out = self._buf("out_tokens", (B, n + 1))
+        ne = self._buf("n_emitted", (B,))
+        check("spec_verify_tree", lib().spec_verify_tree(self.ctx, B, _ptr(seq_ids), n, _ptr(tokens), _ptr(parents),
                                                          _ptr(out), _ptr(ne), _ptr(logits), self.stream.cuda_stream))
         self.leave()
         return out, ne

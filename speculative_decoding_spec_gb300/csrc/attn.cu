@@ -59,10 +59,33 @@ __global__ void embed_rows_kernel(RowsArgs a) {
     if (threadIdx.x == 0) set_error(a.err, SPEC_ERR_TOKEN);
     tok = 0;
   }
-  const int pos = a.seq_len[slot] + i;
+  const int pos = a.seq_len[slot] + i;  // the row's cache slot
+  int rpos = pos;                       // and its position (RoPE)
+  if (a.parents) {
+    // tree verify: row i > 0 is draft node i - 1; its depth below the root
+    // gives its position, its ancestors (and itself, and the root) its mask
+    unsigned int mask = 1u;
+    int depth = 0;
+    if (i > 0) {
+      mask |= 1u << i;
+      depth = 1;
+      int x = a.parents[b * (a.R - 1) + i - 1];
+      for (int guard = 0; x >= 0 && guard < 32; ++guard) {
+        if (x >= i - 1) {  // parents must come earlier; a bad one is treated as the root
+          if (threadIdx.x == 0) set_error(a.err, SPEC_ERR_TOKEN);
+          break;
+        }
+        mask |= 1u << (x + 1);
+        ++depth;
+        x = a.parents[b * (a.R - 1) + x];
+      }
+    }
+    rpos = a.seq_len[slot] + depth;
+    if (threadIdx.x == 0) a.tree_mask[m] = mask;
+  }
   if (threadIdx.x == 0) a.pos[m] = pos;
   for (int c = threadIdx.x; c < a.d; c += blockDim.x) a.x[(size_t)m * a.d + c] = dequant_elem(a.embed, a.d, tok, c);
-  rope_table_row(a.rope_cs + (size_t)m * a.hd, pos, a.hd, a.theta);
+  rope_table_row(a.rope_cs + (size_t)m * a.hd, rpos, a.hd, a.theta);
 }
 
 template <typename KT>
@@ -159,13 +182,14 @@ __global__ void __launch_bounds__(256) attn_page_kernel(AttnArgs a) {
     const int nkeys = L0 + i + a.key_extra;  // keys [0, nkeys)
     const int valid = min(PAGE, nkeys - key0);
     if (valid <= 0) continue;
+    const unsigned int tmask = a.tree_mask ? a.tree_mask[b * a.R + i] : ~0u;
     const float* qv = Qs + q * hd;
     float s[2];
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const int j = lane + 32 * c;
       float acc = 0.f;
-      if (j < valid) {
+      if (j < valid && tree_visible(tmask, L0, key0 + j)) {
         const float* kr = Ks + j * kst;
         for (int d = 0; d < hd; ++d) acc = fmaf(qv[d], kr[d], acc);
         s[c] = acc * scale;
@@ -174,8 +198,8 @@ __global__ void __launch_bounds__(256) attn_page_kernel(AttnArgs a) {
       }
     }
     const float mx = warp_max(fmaxf(s[0], s[1]));
-    const float p0 = lane < valid ? __expf(s[0] - mx) : 0.f;
-    const float p1 = lane + 32 < valid ? __expf(s[1] - mx) : 0.f;
+    const float p0 = s[0] == -INFINITY ? 0.f : __expf(s[0] - mx);
+    const float p1 = s[1] == -INFINITY ? 0.f : __expf(s[1] - mx);
     const float l = warp_sum(p0 + p1);
     const int m = b * a.R + i, h = kvh * G + g;
     const size_t pidx = ((size_t)m * a.nq + h) * a.n_split + pg;
@@ -191,6 +215,35 @@ __global__ void __launch_bounds__(256) attn_page_kernel(AttnArgs a) {
       a.part_ml[pidx * 2 + 0] = mx;
       a.part_ml[pidx * 2 + 1] = l;
     }
+  }
+}
+
+// One CTA per (sequence, layer): the accepted path's rows j = 1..A move from
+// slot L0 + path[j] to L0 + j, in order (path[j] >= j, so no row is
+// overwritten before it is read). Both planes, every KV head.
+__global__ void tree_move_kernel(TreeMoveArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  if (a.err && *(const volatile int*)a.err) return;
+  const int b = blockIdx.x, l = blockIdx.y;
+  const int slot = a.seq_ids[b], n = a.n_emitted[b], A = n - 1;
+  const int L0 = a.seq_len[slot] - n;
+  char* base = (char*)a.pool + (size_t)l * a.layer_elems * a.kv_bytes;
+  const int row_bytes = a.hd * a.kv_bytes;
+  for (int j = 1; j <= A; ++j) {
+    const int src = a.path[b * a.path_ld + j];
+    if (src == j) continue;
+    const int ps = L0 + src, pd = L0 + j;
+    const int gs = a.block_table[(size_t)slot * a.max_pages + ps / PAGE];
+    const int gd = a.block_table[(size_t)slot * a.max_pages + pd / PAGE];
+    if (gs < 0 || gs >= a.n_pages || gd < 0 || gd >= a.n_pages) continue;  // recorded by the pass already
+    for (int e = threadIdx.x; e < 2 * a.nkv * row_bytes / 4; e += blockDim.x) {
+      const int w = e % (row_bytes / 4), ph = e / (row_bytes / 4), plane = ph / a.nkv, h = ph % a.nkv;
+      const size_t so = ((((size_t)gs * 2 + plane) * a.nkv + h) * PAGE + ps % PAGE) * row_bytes;
+      const size_t dof = ((((size_t)gd * 2 + plane) * a.nkv + h) * PAGE + pd % PAGE) * row_bytes;
+      reinterpret_cast<uint32_t*>(base + dof)[w] = reinterpret_cast<const uint32_t*>(base + so)[w];
+    }
+    __syncthreads();
   }
 }
 
@@ -241,6 +294,12 @@ int rope_append(const RopeAppendArgs& a, cudaStream_t st) {
   cudaError_t e = a.kv_dtype == DT_F32 ? cudaLaunchKernelEx(&cfg, rope_append_kernel<float>, a)
                                        : cudaLaunchKernelEx(&cfg, rope_append_kernel<__nv_bfloat16>, a);
   return e == cudaSuccess ? 1 : -1;
+}
+
+int tree_move(const TreeMoveArgs& a, cudaStream_t st) {
+  cudaLaunchAttribute at[1];
+  cudaLaunchConfig_t cfg = pdl_cfg(dim3(a.B, a.L), dim3(256), 0, st, at);
+  return cudaLaunchKernelEx(&cfg, tree_move_kernel, a) == cudaSuccess ? 1 : -1;
 }
 
 size_t attention_smem(int hd, int qn) { return (size_t)(PAGE * (hd + 1) + PAGE * hd + qn * hd) * 4; }

@@ -483,11 +483,13 @@ struct Cta {
     if (t < 32) mu[t] = -INFINITY;
     float mreg[QG];
     int lim[QG];
+    unsigned int tmk[QG];
 #pragma unroll
     for (int q = 0; q < QG; ++q) {
       lsum[q] = 0.f;
       mreg[q] = -INFINITY;
       lim[q] = c0 + q < p.QN ? L0 + (c0 + q) / p.G + a.key_extra : 0;
+      tmk[q] = a.tree_mask && c0 + q < p.QN ? a.tree_mask[w.b * a.R + (c0 + q) / p.G] : ~0u;
     }
     const int key_end = L0 + p.R - 1 + a.key_extra;
     for (int j = 0; j < nb; ++j) {
@@ -502,7 +504,7 @@ struct Cta {
       bool over = false;
 #pragma unroll
       for (int q = 0; q < QG; ++q) {
-        s[q] = key < lim[q] ? (s[q] + lo[q]) * p.scale2 : -INFINITY;
+        s[q] = key < lim[q] && tree_visible(tmk[q], L0, key) ? (s[q] + lo[q]) * p.scale2 : -INFINITY;
         over |= s[q] > mreg[q] + TAU;
       }
       // the running maximum moves (rarely: the first block, or a score 2^8

@@ -116,7 +116,8 @@ struct AttnTc {
   // O += P V. Rows r0 = 16*qt + g and r1 = r0 + 8 of the query tile.
   template <int NT>
   static SPEC_DEV void page_tile(const __nv_bfloat16* Qh, const __nv_bfloat16* Ql, const __nv_bfloat16* Ks,
-                                 const __nv_bfloat16* Vs, int r0, int kb, int key0, int nk0, int nk1, float scale,
+                                 const __nv_bfloat16* Vs, int r0, int kb, int key0, int nk0, int nk1,
+                                 unsigned int tm0, unsigned int tm1, int L0, float scale,
                                  float& m0, float& m1, float& l0, float& l1, float (&o)[NDT][4]) {
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     float s[NT][4];
@@ -149,8 +150,8 @@ struct AttnTc {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int key = key0 + kb + 8 * nt + 2 * c + e;
-        s[nt][e] = key < nk0 ? s[nt][e] * scale : -INFINITY;
-        s[nt][2 + e] = key < nk1 ? s[nt][2 + e] * scale : -INFINITY;
+        s[nt][e] = key < nk0 && tree_visible(tm0, L0, key) ? s[nt][e] * scale : -INFINITY;
+        s[nt][2 + e] = key < nk1 && tree_visible(tm1, L0, key) ? s[nt][2 + e] * scale : -INFINITY;
         mx0 = fmaxf(mx0, s[nt][e]);
         mx1 = fmaxf(mx1, s[nt][2 + e]);
       }
@@ -395,6 +396,8 @@ struct AttnTc {
     const int r0 = 16 * qt + g, r1 = r0 + 8;
     const int nk0 = r0 < QN ? L0 + r0 / G + a.key_extra : 0;
     const int nk1 = r1 < QN ? L0 + r1 / G + a.key_extra : 0;
+    const unsigned int tm0 = a.tree_mask && r0 < QN ? a.tree_mask[b * a.R + r0 / G] : ~0u;
+    const unsigned int tm1 = a.tree_mask && r1 < QN ? a.tree_mask[b * a.R + r1 / G] : ~0u;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     float o[NDT][4];
 #pragma unroll
@@ -417,9 +420,9 @@ struct AttnTc {
         const __nv_bfloat16* Vs = Vb + (size_t)pslot * PAGE * ST;
         const int key0 = (rb + pslot) * PAGE;
         if (KG == 4)
-          page_tile<2>(Qh, Ql, Ks, Vs, r0, 16 * kg, key0, nk0, nk1, scale, m0, m1, l0, l1, o);
+          page_tile<2>(Qh, Ql, Ks, Vs, r0, 16 * kg, key0, nk0, nk1, tm0, tm1, L0, scale, m0, m1, l0, l1, o);
         else
-          page_tile<8>(Qh, Ql, Ks, Vs, r0, 0, key0, nk0, nk1, scale, m0, m1, l0, l1, o);
+          page_tile<8>(Qh, Ql, Ks, Vs, r0, 0, key0, nk0, nk1, tm0, tm1, L0, scale, m0, m1, l0, l1, o);
       }
     }
     __syncthreads();

@@ -47,7 +47,16 @@ struct RopeEpi {
   const int32_t* block_table;
   int* err;
 };
-enum Tail { TAIL_NONE = 0, TAIL_VERIFY = 1, TAIL_PREFILL = 2, TAIL_DRAFT = 3 };
+enum Tail { TAIL_NONE = 0, TAIL_VERIFY = 1, TAIL_PREFILL = 2, TAIL_DRAFT = 3, TAIL_TREE = 4 };
+
+// Tree verify: whether pass row i of a sequence sees key `key`: every committed
+// key (key < L0) and, of the pass's own rows (stored at L0 + row), those set in
+// the row's ancestor mask (bit r: row r is the row itself or an ancestor).
+// mask_i = ~0u outside tree verify (the causal limit alone decides).
+__host__ __device__ inline bool tree_visible(unsigned int mask_i, int L0, int key) {
+  const int r = key - L0;
+  return r < 0 || r >= 32 || ((mask_i >> r) & 1u);
+}
 
 // What the last CTA of an argmax launch does once every row's argmax is known.
 struct TailArgs {
@@ -63,6 +72,9 @@ struct TailArgs {
   int32_t* sel_row;         // [B] pass row whose hidden seeds the drafter
   int32_t* draft_out;       // DRAFT: [B][draft_ld]
   int draft_ld, draft_j;
+  const int32_t* parents;   // TREE: [B][k] parent node of each draft node (-1: the root)
+  int32_t* path;            // TREE: [B][path_ld] rows of the accepted path (root first)
+  int path_ld;
   const int32_t* token_of;  // optional row -> token id map (clustered head)
   unsigned long long* best_all;  // every pass row's packed argmax, zeroed by the last CTA
   unsigned int* counter;    // arrival counter, reset by the last CTA
@@ -109,6 +121,8 @@ struct RowsArgs {
   const int32_t* seq_ids;
   const int32_t* tokens;    // PREFILL: [B][tok_ld], this pass's R from column 0; VERIFY: drafts [B][R-1]
   int tok_ld;               // PREFILL: row stride of tokens (the whole prompt's length)
+  const int32_t* parents;   // tree verify: [B][R-1] parent node of each draft node (-1: the root); else null
+  unsigned int* tree_mask;  // tree verify: [M] ancestor mask of each row (out)
   const int32_t* pending;
   const int32_t* seq_len;
   Mat embed;
@@ -150,6 +164,7 @@ struct AttnArgs {
   const int32_t* seq_ids;
   const int32_t* seq_len;
   const float* rope_cs;     // when non-null, q is rotated on load with [M][hd/2][2]
+  const unsigned int* tree_mask;  // tree verify: [B*R] ancestor mask of each row (tree_visible); else null
   int n_split, pages_per_split;
   float* part_o;            // [M][nq][n_split][hd]
   float* part_ml;           // [M][nq][n_split][2]
@@ -174,6 +189,25 @@ struct TopmArgs {
   int* err;
 };
 int topm_accept(const TopmArgs& a, cudaStream_t st);
+
+// Tree verify: the accepted path's K/V rows (all layers) moved from their
+// pass slots (seq_len_old + row) to consecutive positions (seq_len_old + j).
+// Skipped when the device error word is set (nothing was committed).
+struct TreeMoveArgs {
+  int B, R, L, nkv, hd, kv_bytes;   // kv_bytes: 2 (bf16) or 4 (fp32)
+  const int32_t* seq_ids;
+  const int32_t* seq_len;           // already advanced by A + 1
+  const int32_t* n_emitted;         // [B] A + 1
+  const int32_t* path;              // [B][path_ld]
+  int path_ld;
+  void* pool;
+  long long layer_elems;
+  int max_pages;
+  const int32_t* block_table;
+  int n_pages;
+  const int* err;
+};
+int tree_move(const TreeMoveArgs& a, cudaStream_t st);
 
 // Final-normed hidden state of the row chosen by the accept step -> slot state.
 // Skipped when the device error word `err` is set (the pass commits nothing).

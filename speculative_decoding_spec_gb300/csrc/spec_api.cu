@@ -36,6 +36,8 @@ struct Work {
   unsigned int* counter;
   unsigned int* attn_count;
   float* lg;                // [M][V] row logits (lenient accept)
+  unsigned int* tmask;      // [M] tree verify: ancestor mask per row
+  int32_t* path;            // [B_max][KMAX + 1] tree verify: accepted path rows
   unsigned int *rank, *rank_cnt;
   float* tc_fix;
   unsigned int* tc_cnt;
@@ -92,6 +94,8 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
   w.lg = b.take<float>(base, M * m.vocab);
   w.rank = b.take<unsigned int>(base, (size_t)B_max * KMAX);
   w.rank_cnt = b.take<unsigned int>(base, 4);
+  w.tmask = b.take<unsigned int>(base, M);
+  w.path = b.take<int32_t>(base, (size_t)B_max * (KMAX + 1));
   w.tc_fix = b.take<float>(base, gemv_tc_fixup_bytes() / sizeof(float));
   w.tc_cnt = b.take<unsigned int>(base, tc_counters(m, d));
   w.err = b.take<int>(base, 4);
@@ -257,7 +261,7 @@ AttnWork carve_attention(char* base, int B, int R, int nq, int nkv, int hd, int 
 // ---- the target pass: rows -> layers -> LM head + argmax + accept -----------
 int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, const int32_t* tokens,
                  int32_t* out_tokens, int32_t* n_emitted, float* logits, cudaStream_t st, int top_m = 0,
-                 int tok_ld = 0) {
+                 int tok_ld = 0, const int32_t* parents = nullptr) {
   const spec_model_desc& m = c->m;
   const Work& w = c->wk;
   const int M = B * R, d = m.d_model, hd = m.head_dim, nq = m.n_q_heads, nkv = m.n_kv_heads;
@@ -275,6 +279,7 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
   ra.pending = c->state.pending; ra.seq_len = c->state.seq_len; ra.embed = M_(c->w.embed);
   ra.d = d; ra.hd = hd; ra.theta = m.rope_theta; ra.x = w.x; ra.pos = w.pos; ra.rope_cs = w.rope_cs;
   ra.err = w.err; ra.vocab = m.vocab; ra.tok_ld = tok_ld > 0 ? tok_ld : R;
+  ra.parents = parents; ra.tree_mask = parents ? w.tmask : nullptr;
   LAUNCH(embed_rows(ra, st));
 
   const bool fused_rope = c->fused_rope;
@@ -309,6 +314,7 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     at.block_table = c->kv.block_table; at.seq_ids = seq_ids; at.seq_len = c->state.seq_len;
     at.rope_cs = nullptr; at.n_split = c->kv.max_pages_per_seq; at.pages_per_split = 1;
     at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.att; at.err = w.err;
+    at.tree_mask = parents ? w.tmask : nullptr;
     LAUNCH(run_attention(c, at, st));
 
     g = GemvArgs{};
@@ -341,6 +347,12 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
   t.out_tokens = out_tokens; t.n_emitted = n_emitted; t.seq_len = c->state.seq_len;
   t.pending = c->state.pending; t.stats = c->state.stats; t.sel_row = w.sel_row;
   t.best_all = w.best; t.counter = w.counter; t.err = w.err;
+  if (parents) {
+    t.mode = TAIL_TREE;
+    t.parents = parents;
+    t.path = w.path;
+    t.path_ld = KMAX + 1;
+  }
   if (top_m > 0) {
     // lenient accept: every row's logits kept, the accept runs in its own kernel
     if (!g.Y) g.Y = w.lg;
@@ -356,6 +368,15 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     LAUNCH(topm_accept(ta, st));
   }
   LAUNCH(commit_hidden(B, seq_ids, w.sel_row, w.x, d, c->w.g_final, m.rms_eps, c->state.hid, w.err, st));
+  if (parents) {
+    TreeMoveArgs tm = {};
+    tm.B = B; tm.R = R; tm.L = m.n_layers; tm.nkv = nkv; tm.hd = hd; tm.kv_bytes = m.kv_dtype == SPEC_F32 ? 4 : 2;
+    tm.seq_ids = seq_ids; tm.seq_len = c->state.seq_len; tm.n_emitted = n_emitted; tm.path = w.path;
+    tm.path_ld = KMAX + 1; tm.pool = c->kv.pool; tm.layer_elems = c->layer_elems;
+    tm.max_pages = c->kv.max_pages_per_seq; tm.block_table = c->kv.block_table; tm.n_pages = c->kv.n_pages;
+    tm.err = w.err;
+    LAUNCH(tree_move(tm, st));
+  }
   return n;
 }
 
@@ -633,6 +654,23 @@ spec_status spec_verify_topm(spec_ctx* c, int32_t B, const int32_t* seq_ids, int
                    st, [&](cudaStream_t s) {
                      return enqueue_pass(c, B, seq_ids, k + 1, TAIL_VERIFY, drafts, out_tokens, n_emitted,
                                          logits_dbg, s, top_m);
+                   });
+}
+
+spec_status spec_verify_tree(spec_ctx* c, int32_t B, const int32_t* seq_ids, int32_t n, const int32_t* tokens,
+                             const int32_t* parents, int32_t* out_tokens, int32_t* n_emitted, float* logits_dbg,
+                             void* stream) {
+  if (!batch_ok(c, B, seq_ids) || n < 1 || n > KMAX || n + 1 > c->pass_rows || !tokens || !parents || !out_tokens ||
+      !n_emitted)
+    return SPEC_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  return run_graph(c,
+                   key_of("verify_tree", {B, n, (long long)seq_ids, (long long)tokens, (long long)parents,
+                                          (long long)out_tokens, (long long)n_emitted, (long long)logits_dbg,
+                                          (long long)st}),
+                   st, [&](cudaStream_t s) {
+                     return enqueue_pass(c, B, seq_ids, n + 1, TAIL_VERIFY, tokens, out_tokens, n_emitted,
+                                         logits_dbg, s, 0, 0, parents);
                    });
 }
 
