@@ -72,13 +72,24 @@ typedef struct {
 
 /* Target decoder: pre-norm layers of RMSNorm -> QKV -> RoPE -> causal GQA
  * attention -> O (+residual), RMSNorm -> gate/up -> GELU(gate)*up -> down
- * (+residual); final RMSNorm; LM head tied to the embedding. */
+ * (+residual); final RMSNorm; LM head tied to the embedding.
+ * Mixture of experts (n_experts > 0; "Gemma 4 acceleration: faster inference
+ * with multi-token prediction drafters" (cafe.daangn.com), section "MTP drafter
+ * internal optimisations" names a 26B mixture-of-experts target without its
+ * layer): the FFN becomes router scores W_r . xn over n_experts experts, each
+ * row's top_k experts by score (ties to the lower id), softmax weights over
+ * the chosen scores, and a gated-GELU FFN of width d_ff_expert per expert,
+ * y = sum of weight * expert(xn). top_k <= 8, n_experts <= 256; f32 or bf16
+ * weights. */
 typedef struct {
     int32_t n_layers, d_model, n_q_heads, n_kv_heads, head_dim, d_ff, vocab;
     int32_t w_dtype;     /* spec_dtype of every matrix, embedding included  */
     int32_t kv_dtype;    /* SPEC_F32 or SPEC_BF16                           */
     float rms_eps;       /* 1e-6                                            */
     float rope_theta;    /* 10000, rotate-half pairing                      */
+    int32_t n_experts;   /* 0: dense FFN                                    */
+    int32_t top_k;       /* experts per row (mixture of experts)            */
+    int32_t d_ff_expert; /* width of one expert's FFN                       */
 } spec_model_desc;
 
 typedef struct {
@@ -90,6 +101,9 @@ typedef struct {
     const float *g_attn; /* [n_layers][d_model] RMSNorm gains                */
     const float *g_ffn;  /* [n_layers][d_model]                              */
     const float *g_final;/* [d_model]                                        */
+    spec_matrix router;  /* mixture of experts: n_layers x [n_experts][d_model] */
+    spec_matrix wgu_e;   /* (n_layers * n_experts) x [2*d_ff_expert][d_model]: gate rows, up rows */
+    spec_matrix wdown_e; /* (n_layers * n_experts) x [d_model][d_ff_expert]  */
 } spec_weights;
 
 /* Drafter head ("Gemma 4's MTP drafter explained", section "What is different

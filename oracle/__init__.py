@@ -49,6 +49,7 @@ def lib():
         _lib.or_rank_f32.argtypes = [p, i, i]
         _lib.or_verify_topm.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), i, p, i, p, p, p, p]
         _lib.or_verify_tree.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), i, p, p, p, p, p]
+        _lib.or_topk_f32.argtypes = [p, i, i, p, p]
         _lib.or_greedy.argtypes = [C.POINTER(OrModel), C.POINTER(OrSeq), i, p, p]
         _lib.or_draft.argtypes = [C.POINTER(OrModel), C.POINTER(OrDrafter), C.POINTER(OrSeq), i,
                                   p, p]
@@ -65,7 +66,8 @@ class OrModel(C.Structure):
     _fields_ = [(n, C.c_int) for n in ("L", "d", "nq", "nkv", "hd", "ff", "V", "kv_dtype")] + [
         ("eps", C.c_double), ("theta", C.c_double), ("embed", OrW), ("wqkv", OrW), ("wo", OrW),
         ("wgu", OrW), ("wdown", OrW), ("g_attn", C.c_void_p), ("g_ffn", C.c_void_p),
-        ("g_final", C.c_void_p)]
+        ("g_final", C.c_void_p), ("n_experts", C.c_int), ("top_k", C.c_int), ("ff_e", C.c_int),
+        ("router", OrW), ("wgu_e", OrW), ("wdown_e", OrW)]
 
 
 class OrDrafter(C.Structure):
@@ -127,6 +129,9 @@ class Target:
                          embed=k.w(tw.embed), wqkv=k.w(tw.wqkv), wo=k.w(tw.wo), wgu=k.w(tw.wgu),
                          wdown=k.w(tw.wdown), g_attn=_ptr(k.arr(tw.g_attn)),
                          g_ffn=_ptr(k.arr(tw.g_ffn)), g_final=_ptr(k.arr(tw.g_final)))
+        if getattr(s, "n_experts", 0):
+            self.m.n_experts, self.m.top_k, self.m.ff_e = s.n_experts, s.top_k, s.ff_e
+            self.m.router, self.m.wgu_e, self.m.wdown_e = k.w(tw.router), k.w(tw.wgu_e), k.w(tw.wdown_e)
 
 
 class Drafter:
@@ -267,6 +272,14 @@ def verify_tree(t: Target, s: Seq, tokens, parents):
     rc = lib().or_verify_tree(C.byref(t.m), C.byref(s.c), n, _ptr(tk), _ptr(pa), _ptr(out), _ptr(ne), _ptr(mg))
     assert rc == 0, "or_verify_tree failed (bad parents or capacity)"
     return out[: ne[0]].copy(), mg
+
+
+def topk_f32(scores, k: int):
+    sc = np.ascontiguousarray(np.asarray(scores, np.float64))
+    idx = np.zeros(k, np.int32)
+    gap = C.c_double()
+    lib().or_topk_f32(_ptr(sc), sc.shape[0], k, _ptr(idx), C.addressof(gap))
+    return idx, gap.value
 
 
 def rank_f32(logits, tok: int) -> int:

@@ -216,6 +216,70 @@ int or_argmax_f32(const double *logits, int n, double *margin)
     return best;
 }
 
+void or_topk_f32(const double *scores, int n, int k, int32_t *idx, double *gap)
+{
+    char *taken = (char *)calloc((size_t)n, 1);
+    for (int j = 0; j < k; ++j) {
+        int best = -1;
+        for (int i = 0; i < n; ++i)
+            if (!taken[i] && (best < 0 || (float)scores[i] > (float)scores[best]))
+                best = i;
+        taken[best] = 1;
+        idx[j] = best;
+    }
+    if (gap) {
+        double lo_in = INFINITY, hi_out = -INFINITY;
+        for (int i = 0; i < n; ++i) {
+            if (taken[i] && scores[i] < lo_in)
+                lo_in = scores[i];
+            if (!taken[i] && scores[i] > hi_out)
+                hi_out = scores[i];
+        }
+        *gap = lo_in - hi_out;
+    }
+    free(taken);
+}
+
+/* Mixture-of-experts FFN of one row ([P1 "MTP drafter internal
+ * optimisations"]: a 26B mixture-of-experts target, whose routing makes batch
+ * 1 the hard case; the pages give no layer definition). Reading: router
+ * scores z = W_r . xn; the top_k experts by binary32 score (ties to the lower
+ * id); weights = softmax of their scores; each expert is the gated-GELU FFN
+ * of the dense layer with its own width ff_e. */
+void or_moe_ffn(const or_model *m, int l, const double *xn, double *y)
+{
+    const int d = m->d, E = m->n_experts, K = m->top_k, ff = m->ff_e;
+    double *z = (double *)malloc(sizeof(double) * (size_t)E);
+    int32_t *sel = (int32_t *)malloc(sizeof(int32_t) * (size_t)K);
+    double *gu = (double *)malloc(sizeof(double) * (size_t)2 * ff);
+    double *act = (double *)malloc(sizeof(double) * (size_t)ff);
+    double *out = (double *)malloc(sizeof(double) * (size_t)d);
+    or_w r = layer_slice(&m->router, l, E, d);
+    or_linear(&r, E, d, xn, 1, z);
+    or_topk_f32(z, E, K, sel, NULL);
+    double mx = -INFINITY, tot = 0.0;
+    for (int j = 0; j < K; ++j)
+        if (z[sel[j]] > mx)
+            mx = z[sel[j]];
+    for (int j = 0; j < K; ++j)
+        tot += exp(z[sel[j]] - mx);
+    for (int i = 0; i < d; ++i)
+        y[i] = 0.0;
+    for (int j = 0; j < K; ++j) {
+        const int e = sel[j];
+        const double wgt = exp(z[e] - mx) / tot;
+        or_w g = layer_slice(&m->wgu_e, l * E + e, 2 * ff, d);
+        or_linear(&g, 2 * ff, d, xn, 1, gu);
+        for (int i = 0; i < ff; ++i)
+            act[i] = or_gelu(gu[i]) * gu[ff + i];
+        or_w dn = layer_slice(&m->wdown_e, l * E + e, d, ff);
+        or_linear(&dn, d, ff, act, 1, out);
+        for (int i = 0; i < d; ++i)
+            y[i] += wgt * out[i];
+    }
+    free(z); free(sel); free(gu); free(act); free(out);
+}
+
 /* ------------------------------------------------------------------ */
 /* target model                                                        */
 /* ------------------------------------------------------------------ */
@@ -294,6 +358,14 @@ int or_forward_resid(const or_model *m, or_seq *s, const int32_t *tokens, int R,
         for (int r = 0; r < R; ++r)
             or_rmsnorm(x + (int64_t)r * d, d, m->g_ffn + (int64_t)l * d, m->eps,
                        xn + (int64_t)r * d);
+        if (m->n_experts > 0) {
+            for (int r = 0; r < R; ++r) {
+                or_moe_ffn(m, l, xn + (int64_t)r * d, tmp + (int64_t)r * d);
+                for (int i = 0; i < d; ++i)
+                    x[(int64_t)r * d + i] += tmp[(int64_t)r * d + i];
+            }
+            continue;
+        }
         w = layer_slice(&m->wgu, l, 2 * ff, d);
         or_linear(&w, 2 * ff, d, xn, R, gu);
         for (int r = 0; r < R; ++r)

@@ -59,6 +59,11 @@ typedef struct {
     const float *g_attn;     /* [L][d] */
     const float *g_ffn;      /* [L][d] */
     const float *g_final;    /* [d] */
+    /* mixture of experts (n_experts = 0: the dense FFN above) */
+    int n_experts, top_k, ff_e;
+    or_w router;             /* L x [n_experts][d] */
+    or_w wgu_e;              /* L x n_experts x [2*ff_e][d]: gate rows then up rows */
+    or_w wdown_e;            /* L x n_experts x [d][ff_e] */
 } or_model;
 
 typedef struct {
@@ -105,6 +110,13 @@ double or_gelu(double x);
 void   or_attend(const double *q, const float *K, const float *V, int n_keys,
                  int hd, double *o);
 int    or_argmax_f32(const double *logits, int n, double *margin);
+/* The k largest of n binary32-rounded scores (ties: lower index first), in
+ * order; gap (optional) = smallest distance between a chosen and an unchosen
+ * score. */
+void   or_topk_f32(const double *scores, int n, int k, int32_t *idx, double *gap);
+/* One row through a mixture-of-experts FFN layer l: y = sum over the row's
+ * top_k experts (router scores on xn) of softmax-weight * expert FFN(xn). */
+void   or_moe_ffn(const or_model *m, int l, const double *xn, double *y);
 
 /* ---- target model ---- */
 /* Forward R rows of one sequence at positions len..len+R-1 (causal). Writes

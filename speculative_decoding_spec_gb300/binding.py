@@ -36,13 +36,15 @@ class spec_matrix(C.Structure):
 class spec_model_desc(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("n_layers", "d_model", "n_q_heads", "n_kv_heads", "head_dim",
                                           "d_ff", "vocab", "w_dtype", "kv_dtype")] + [
-        ("rms_eps", C.c_float), ("rope_theta", C.c_float)]
+        ("rms_eps", C.c_float), ("rope_theta", C.c_float), ("n_experts", C.c_int32), ("top_k", C.c_int32),
+        ("d_ff_expert", C.c_int32)]
 
 
 class spec_weights(C.Structure):
     _fields_ = [("embed", spec_matrix), ("wqkv", spec_matrix), ("wo", spec_matrix), ("wgu", spec_matrix),
                 ("wdown", spec_matrix), ("g_attn", C.c_void_p), ("g_ffn", C.c_void_p),
-                ("g_final", C.c_void_p)]
+                ("g_final", C.c_void_p), ("router", spec_matrix), ("wgu_e", spec_matrix),
+                ("wdown_e", spec_matrix)]
 
 
 class spec_drafter_desc(C.Structure):
@@ -155,7 +157,8 @@ def _mat(w) -> spec_matrix:
 
 def model_desc(t) -> spec_model_desc:
     return spec_model_desc(t.L, t.d, t.nq, t.nkv, t.hd, t.ff, t.V, DTYPES[t.wdtype], DTYPES[t.kvdtype],
-                           t.eps, t.theta)
+                           t.eps, t.theta, getattr(t, "n_experts", 0), getattr(t, "top_k", 0),
+                           getattr(t, "ff_e", 0))
 
 
 def drafter_desc(d) -> spec_drafter_desc:
@@ -257,8 +260,11 @@ class Engine:
         self.n_slots, self.B_max, self.rows_max = n_slots, B_max, rows_max
         self.stream = torch.cuda.Stream(device=device)
         self._md = model_desc(t)
+        moe = getattr(tw, "router", None) is not None
         self._w = spec_weights(_mat(tw.embed), _mat(tw.wqkv), _mat(tw.wo), _mat(tw.wgu), _mat(tw.wdown),
-                               _ptr(tw.g_attn), _ptr(tw.g_ffn), _ptr(tw.g_final))
+                               _ptr(tw.g_attn), _ptr(tw.g_ffn), _ptr(tw.g_final),
+                               _mat(tw.router) if moe else spec_matrix(), _mat(tw.wgu_e) if moe else spec_matrix(),
+                               _mat(tw.wdown_e) if moe else spec_matrix())
         self._dd = self._dw = None
         if dw is not None:
             self._dd = drafter_desc(dw.shape)

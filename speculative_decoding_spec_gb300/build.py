@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspec_gb300.so")
-SOURCES = ["gemv.cu", "gemv_tc.cu", "gemm_wide.cu", "attn.cu", "attn_tc.cu", "attn_flash.cu", "draft.cu", "spec_api.cu", "accept_topm.cu", "linear_noalloc.cu"]
+SOURCES = ["gemv.cu", "gemv_tc.cu", "gemm_wide.cu", "attn.cu", "attn_tc.cu", "attn_flash.cu", "draft.cu", "spec_api.cu", "accept_topm.cu", "moe.cu", "linear_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

@@ -29,6 +29,9 @@ class TargetShape:
     wstd: float
     eps: float = 1e-6
     theta: float = 10000.0
+    n_experts: int = 0            # mixture of experts: experts per layer (0: dense FFN)
+    top_k: int = 0                # experts each row uses
+    ff_e: int = 0                 # width of one expert's FFN
 
     @property
     def nqkv(self) -> int:
@@ -37,7 +40,8 @@ class TargetShape:
     def weight_bytes(self) -> int:
         """Bytes of every linear weight plus the tied embedding / LM head."""
         per = {F32: 4.0, BF16: 2.0, Q4_0: 0.5 + 2.0 / 32}[self.wdtype]
-        layer = self.d * self.nqkv + self.d * self.nq * self.hd + 3 * self.d * self.ff
+        ffn = 3 * self.d * self.ff if not self.n_experts else self.n_experts * (3 * self.d * self.ff_e + self.d)
+        layer = self.d * self.nqkv + self.d * self.nq * self.hd + ffn
         return int(round((self.L * layer + self.V * self.d) * per))
 
     def kv_bytes_per_pos(self) -> int:
@@ -99,6 +103,16 @@ E4B = TargetShape(L=32, d=2560, nq=20, nkv=4, hd=128, ff=10240, V=262144, wdtype
 DENSE30B = TargetShape(L=48, d=6144, nq=48, nkv=8, hd=128, ff=24576, V=262144, wdtype=BF16,
                        kvdtype=BF16, wstd=0.01)
 
+# Mixture-of-experts targets ("Gemma 4 acceleration: faster inference with
+# multi-token prediction drafters" (cafe.daangn.com), "MTP drafter internal
+# optimisations": a 26B mixture-of-experts model, little gain at batch 1 because
+# of routing, about 2.2x at batch 4-8). The pages give no layer shapes: these
+# are synthetic, with each row using top_k of n_experts gated-GELU experts.
+TINY_MOE = TargetShape(L=2, d=256, nq=4, nkv=4, hd=64, ff=256, V=4096, wdtype=F32, kvdtype=F32, wstd=0.02,
+                       n_experts=8, top_k=2, ff_e=256)
+MOE = TargetShape(L=16, d=2048, nq=16, nkv=8, hd=128, ff=1024, V=262144, wdtype=BF16, kvdtype=BF16,
+                  wstd=0.02, n_experts=64, top_k=4, ff_e=1024)
+
 WORKLOADS = {
     "tiny_f32_b1_k3": Workload("tiny_f32_b1_k3", TINY, _drafter(TINY, 1, 64, False), B=1,
                                ctx=(64, 64), k=3, alphas=(), prompt=True, steps=16),
@@ -118,6 +132,8 @@ WORKLOADS = {
     "dense30b_bf16_b8_ctx8192_k4": Workload("dense30b_bf16_b8_ctx8192_k4", DENSE30B,
                                             _drafter(DENSE30B, 4, 256, True), B=8,
                                             ctx=(8192, 8192), k=4, alphas=(0.5, 0.8)),
+    "moe_bf16_b8_ctx4096_k4": Workload("moe_bf16_b8_ctx4096_k4", MOE, _drafter(MOE, 4, 256, True), B=8,
+                                       ctx=(4096, 4096), k=4, alphas=(0.7,)),
 }
 
 BENCH_WORKLOAD = "dense30b_bf16_b8_ctx8192_k4"

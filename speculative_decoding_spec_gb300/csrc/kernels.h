@@ -209,6 +209,26 @@ struct TreeMoveArgs {
 };
 int tree_move(const TreeMoveArgs& a, cudaStream_t st);
 
+// Mixture-of-experts FFN (moe.cu) of M pass rows: routing of the router scores
+// z, grouped expert projections over the rows routed to each expert, and the
+// weighted combine into the residual x.
+struct MoeArgs {
+  int M, E, K, d, ff;          // rows, experts, experts per row, width, expert FFN width
+  const float* xn;             // [M][d] normalised rows (FFN gain applied)
+  const float* z;              // [M][E] router scores
+  int32_t* sel;                // [M][K] chosen experts
+  float* wts;                  // [M][K] their softmax weights
+  int32_t* cnt;                // [E] rows per expert
+  int32_t* list;               // [E][M] selections (row * K + slot) per expert, row order
+  float* act;                  // [M*K][ff] expert intermediates per selection
+  float* out;                  // [M*K][d] expert outputs per selection
+  float* x;                    // [M][d] residual (in/out)
+};
+void setup_moe_attributes();
+size_t moe_smem(int d, int ff);
+int moe_ffn(const MoeArgs& a, const void* wgu_layer, const void* wdown_layer, int wdtype, cudaStream_t st);
+int rmsnorm_rows(const float* x, int M, int d, const float* g, float eps, float* xn, cudaStream_t st);
+
 // Final-normed hidden state of the row chosen by the accept step -> slot state.
 // Skipped when the device error word `err` is set (the pass commits nothing).
 int commit_hidden(int B, const int32_t* seq_ids, const int32_t* sel_row, const float* x, int d,

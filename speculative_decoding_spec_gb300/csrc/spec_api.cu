@@ -36,6 +36,7 @@ struct Work {
   unsigned int* counter;
   unsigned int* attn_count;
   float* lg;                // [M][V] row logits (lenient accept)
+  MoeArgs moe;              // mixture-of-experts buffers (null fields for a dense target)
   unsigned int* tmask;      // [M] tree verify: ancestor mask per row
   int32_t* path;            // [B_max][KMAX + 1] tree verify: accepted path rows
   unsigned int *rank, *rank_cnt;
@@ -95,6 +96,18 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
   w.rank = b.take<unsigned int>(base, (size_t)B_max * KMAX);
   w.rank_cnt = b.take<unsigned int>(base, 4);
   w.tmask = b.take<unsigned int>(base, M);
+  if (m.n_experts > 0) {
+    const int E = m.n_experts, K = m.top_k, ff = m.d_ff_expert;
+    w.moe.E = E; w.moe.K = K; w.moe.d = m.d_model; w.moe.ff = ff;
+    w.moe.xn = b.take<float>(base, M * m.d_model);
+    w.moe.z = b.take<float>(base, M * E);
+    w.moe.sel = b.take<int32_t>(base, M * K);
+    w.moe.wts = b.take<float>(base, M * K);
+    w.moe.cnt = b.take<int32_t>(base, E);
+    w.moe.list = b.take<int32_t>(base, (size_t)E * M);
+    w.moe.act = b.take<float>(base, M * K * ff);
+    w.moe.out = b.take<float>(base, M * K * m.d_model);
+  }
   w.path = b.take<int32_t>(base, (size_t)B_max * (KMAX + 1));
   w.tc_fix = b.take<float>(base, gemv_tc_fixup_bytes() / sizeof(float));
   w.tc_cnt = b.take<unsigned int>(base, tc_counters(m, d));
@@ -146,6 +159,10 @@ bool mat_ok(const spec_matrix& mm, int K) {
 Mat M_(const spec_matrix& m) { return Mat{m.dtype, m.data, m.scales}; }
 
 bool model_ok(const spec_model_desc& m) {
+  if (m.n_experts < 0 || (m.n_experts > 0 && (m.n_experts > 256 || m.top_k < 1 || m.top_k > 8 ||
+                                               m.top_k > m.n_experts || m.d_ff_expert <= 0 ||
+                                               m.d_ff_expert % 8 || m.w_dtype == SPEC_Q4_0)))
+    return false;
   return m.n_layers > 0 && m.d_model > 0 && m.n_q_heads > 0 && m.n_kv_heads > 0 && m.head_dim > 0 &&
          m.head_dim % 2 == 0 && m.head_dim <= 256 && m.n_q_heads % m.n_kv_heads == 0 && m.d_ff > 0 &&
          m.vocab > 1 && (m.kv_dtype == SPEC_F32 || m.kv_dtype == SPEC_BF16) && m.d_model % 8 == 0 &&
@@ -234,6 +251,7 @@ void spec::setup_device_attributes() {
   setup_attn_tc_attributes();
   setup_draft_attributes();
   setup_attn_flash_attributes();
+  setup_moe_attributes();
   done[dev] = true;
 }
 
@@ -323,6 +341,23 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     g.epi = EPI_ADD; g.Y = w.x; g.ldy = d; g.pdl = 1;
     LAUNCH(run_gemv(c, g, st));
 
+    if (m.n_experts > 0) {
+      // mixture of experts: normalised rows, router scores, routing, grouped
+      // experts, weighted combine into the residual
+      const int E = m.n_experts, ffe = m.d_ff_expert;
+      MoeArgs ma = w.moe;
+      ma.M = M; ma.x = w.x;
+      LAUNCH(rmsnorm_rows(w.x, M, d, c->w.g_ffn + (size_t)l * d, m.rms_eps, const_cast<float*>(ma.xn), st));
+      g = GemvArgs{};
+      g.X = ma.xn; g.ldx = d; g.M = M; g.N = E; g.K = d;
+      g.W = mat_layer(M_(c->w.router), l, E, d);
+      g.epi = EPI_STORE; g.Y = const_cast<float*>(ma.z); g.ldy = E; g.pdl = 1;
+      LAUNCH(run_gemv(c, g, st));
+      const Mat gu = mat_layer(M_(c->w.wgu_e), l * E, 2 * ffe, d);
+      const Mat dn = mat_layer(M_(c->w.wdown_e), l * E, d, ffe);
+      LAUNCH(moe_ffn(ma, gu.data, dn.data, m.w_dtype == SPEC_F32 ? DT_F32 : DT_BF16, st));
+      continue;
+    }
     g = GemvArgs{};
     g.X = w.x; g.ldx = d; g.M = M; g.N = 2 * ff; g.K = d;
     g.W = mat_layer(M_(c->w.wgu), l, 2 * ff, d);
@@ -554,10 +589,15 @@ spec_status spec_init(const spec_model_desc* model, const spec_weights* weights,
   if (!state->seq_len || !state->pending || !state->hid || !state->stats) return SPEC_EINVAL;
   const int nqkv = (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim, qd = m.n_q_heads * m.head_dim;
   const spec_weights& w = *weights;
-  if (!mat_ok(w.embed, m.d_model) || !mat_ok(w.wqkv, m.d_model) || !mat_ok(w.wo, qd) ||
-      !mat_ok(w.wgu, m.d_model) || !mat_ok(w.wdown, m.d_ff) || !w.g_attn || !w.g_ffn || !w.g_final)
+  if (!mat_ok(w.embed, m.d_model) || !mat_ok(w.wqkv, m.d_model) || !mat_ok(w.wo, qd) || !w.g_attn || !w.g_ffn ||
+      !w.g_final)
     return SPEC_EINVAL;
-  for (const spec_matrix* mm : {&w.embed, &w.wqkv, &w.wo, &w.wgu, &w.wdown})
+  if (m.n_experts == 0 && (!mat_ok(w.wgu, m.d_model) || !mat_ok(w.wdown, m.d_ff))) return SPEC_EINVAL;
+  if (m.n_experts > 0 && (!mat_ok(w.router, m.d_model) || !mat_ok(w.wgu_e, m.d_model) ||
+                          !mat_ok(w.wdown_e, m.d_ff_expert) || w.router.dtype != m.w_dtype ||
+                          w.wgu_e.dtype != m.w_dtype || w.wdown_e.dtype != m.w_dtype))
+    return SPEC_EINVAL;
+  for (const spec_matrix* mm : {&w.embed, &w.wqkv, &w.wo})
     if (mm->dtype != m.w_dtype) return SPEC_EINVAL;
   (void)nqkv;
   const int G = m.n_q_heads / m.n_kv_heads;

@@ -8,6 +8,8 @@ available, so these stand in for the pages' coding / summarisation prompts):
 * linear weights, embedding (tied LM head) and drafter tables: N(0, wstd),
   wstd = 0.02 (0.01 for the ~30B model), stored in the model's weight dtype;
   Q4_0 weights: codes uniform on 0..15, fp16 scales |N(0, 0.004)|;
+* mixture-of-experts targets: router and expert matrices N(0, wstd) like the
+  rest (the dense FFN matrices are then small placeholders, unused);
 * norm gains: 1 + N(0, 0.1) per element, from their own seeded stream (so that
   a gain read from the wrong layer or the wrong norm changes the result);
 * the drafter's clustered vocabulary: a random permutation of the token ids
@@ -110,9 +112,13 @@ class TargetWeights:
     g_attn: torch.Tensor    # f32 [L][d]
     g_ffn: torch.Tensor     # f32 [L][d]
     g_final: torch.Tensor   # f32 [d]
+    router: Optional[WTensor] = None    # mixture of experts: L x [E][d]
+    wgu_e: Optional[WTensor] = None     # (L*E) x [2 ff_e][d]: gate rows then up rows
+    wdown_e: Optional[WTensor] = None   # (L*E) x [d][ff_e]
 
     def matrices(self) -> List[WTensor]:
-        return [self.embed, self.wqkv, self.wo, self.wgu, self.wdown]
+        m = [self.embed, self.wqkv, self.wo, self.wgu, self.wdown]
+        return m + ([self.router, self.wgu_e, self.wdown_e] if self.router is not None else [])
 
 
 def make_target(t: TargetShape, device="cpu", seed=SEED_WEIGHTS) -> TargetWeights:
@@ -121,11 +127,20 @@ def make_target(t: TargetShape, device="cpu", seed=SEED_WEIGHTS) -> TargetWeight
     embed = w(1, t.V, t.d)
     wqkv = w(t.L, t.nqkv, t.d)
     wo = w(t.L, t.d, t.nq * t.hd)
-    wgu = w(t.L, 2 * t.ff, t.d)
-    wdown = w(t.L, t.d, t.ff)
+    if t.n_experts:
+        # mixture of experts: no dense FFN; router and experts drawn like the rest
+        wgu = w(t.L, 8, t.d)
+        wdown = w(t.L, t.d, 8)
+        router = w(t.L, t.n_experts, t.d)
+        wgu_e = w(t.L * t.n_experts, 2 * t.ff_e, t.d)
+        wdown_e = w(t.L * t.n_experts, t.d, t.ff_e)
+    else:
+        wgu = w(t.L, 2 * t.ff, t.d)
+        wdown = w(t.L, t.d, t.ff)
+        router = wgu_e = wdown_e = None
     gains = _gains(seed + SEED_GAINS, device)
     return TargetWeights(t, embed, wqkv, wo, wgu, wdown, gains(t.L, t.d), gains(t.L, t.d),
-                         gains(t.d))
+                         gains(t.d), router, wgu_e, wdown_e)
 
 
 @dataclass

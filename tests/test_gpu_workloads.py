@@ -92,7 +92,7 @@ def _injected_steps(eng, ids, w, ref, steps, alpha, seed_off=0):
 
 
 LARGE = [n for n, w in configs.WORKLOADS.items() if not w.prompt]
-SAMPLE = {"e2b_q4_0_b4_ctx4096_k4": [1, 3], "e4b_bf16_b8_ragged_k4": [0, 5],
+SAMPLE = {"e2b_q4_0_b4_ctx4096_k4": [1, 3], "e4b_bf16_b8_ragged_k4": [0, 5], "moe_bf16_b8_ctx4096_k4": [2],
           "dense30b_bf16_b8_ctx8192_k4": [6]}
 # tokens compared against the oracle's free-running greedy decode (one oracle
 # target pass per token; a ~30B-class pass takes seconds on the host cores)
