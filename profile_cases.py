@@ -29,6 +29,16 @@ Each summary under profiles/ names the case and the ncu command it ran.
     python profile_cases.py attention_30b
         the verify attention of the ~30B-class model at batch 8, context
         8192, k = 4 (one layer's cache: 268 MB), three launches.
+    python profile_cases.py lmhead_30b
+        the ~30B-class model's LM head (262144 x 6144 bf16, 3.2 GB) at M = 40
+        rows, twice.
+    python profile_cases.py step_30b_b8
+        the bench's workload (~30B-class bf16, batch 8, context 8192, k = 4):
+        two speculative steps (draft, then verify) inside an NVTX range
+        "step" after the set-up (about 70 GB on the device).
+    python profile_cases.py verify_moe
+        the mixture-of-experts workload (batch 8, context 4096, k = 4): two
+        verify passes inside an NVTX range "verify".
 
 Inputs are the seeded synthetic weights and caches of the workloads; nothing
 here checks results (the tests do).
@@ -135,9 +145,45 @@ def attention_30b(w):
     torch.cuda.synchronize()
 
 
+def lmhead_30b(w):
+    t = configs.DENSE30B
+    g = torch.Generator(device="cuda").manual_seed(6)
+    W = synth.make_matrix(g, t.wdtype, 1, t.V, t.d, t.wstd, "cuda")
+    x = torch.randn((40, t.d), device="cuda")
+    y = torch.empty((40, t.V), device="cuda")
+    for _ in range(2):
+        binding.spec_linear(W, x, y=y)
+    torch.cuda.synchronize()
+
+
+def _steps(w, nvtx, n, draft=True):
+    _, eng, ids = _engine(w)
+    d0 = eng._in("d0", torch.arange(1, 1 + w.B * w.k, dtype=torch.int32).view(w.B, w.k))
+    # one untimed round so that every call shape is captured before the range
+    if draft:
+        eng.spec_draft(ids, w.B, w.k)
+    eng.spec_verify(ids, d0)
+    eng.sync()
+    torch.cuda.nvtx.range_push(nvtx)
+    for _ in range(n):
+        d = eng.spec_draft(ids, w.B, w.k) if draft else d0
+        eng.spec_verify(ids, d)
+    eng.sync()
+    torch.cuda.nvtx.range_pop()
+
+
+def step_30b_b8(w):
+    _steps(configs.WORKLOADS["dense30b_bf16_b8_ctx8192_k4"], "step", 2)
+
+
+def verify_moe(w):
+    _steps(configs.WORKLOADS["moe_bf16_b8_ctx4096_k4"], "verify", 2, draft=False)
+
+
 CASES = {"projections": projections, "projections_wide": projections_wide, "projections_30b": projections_30b,
          "projections_30b_m5": projections_30b_m5, "projections_wide_q4": projections_wide_q4,
-         "verify_q4b4": verify_q4b4, "draft": draft, "verify": verify, "attention_30b": attention_30b}
+         "verify_q4b4": verify_q4b4, "draft": draft, "verify": verify, "attention_30b": attention_30b,
+         "lmhead_30b": lmhead_30b, "step_30b_b8": step_30b_b8, "verify_moe": verify_moe}
 
 
 def main(argv):
