@@ -13,6 +13,9 @@ Each summary under profiles/ names the case and the ncu command it ran.
         one layer of the ~30B-class bf16 target (QKV, O, gate/up, down: 1.08
         GB) at M = 40 rows (batch 8, k = 4), run twice: the per-layer matrix
         shapes of the bench's roofline kernel.
+    python profile_cases.py layer_and_head_30b
+        the same layer followed by the LM head (262144 x 6144 bf16, 3.2 GB),
+        run twice: one of each projection shape of a verify pass.
     python profile_cases.py projections_30b_m5
         the same shapes at M = 5 rows (batch 1, k = 4).
     python profile_cases.py projections_wide_q4
@@ -102,6 +105,10 @@ def projections_30b(w):
     _one_layer_and_head(configs.DENSE30B, 40, 5, head=False)
 
 
+def layer_and_head_30b(w):
+    _one_layer_and_head(configs.DENSE30B, 40, 5, head=True)
+
+
 def projections_30b_m5(w):
     _one_layer_and_head(configs.DENSE30B, 5, 5, head=False)
 
@@ -181,6 +188,7 @@ def verify_moe(w):
 
 
 CASES = {"projections": projections, "projections_wide": projections_wide, "projections_30b": projections_30b,
+         "layer_and_head_30b": layer_and_head_30b,
          "projections_30b_m5": projections_30b_m5, "projections_wide_q4": projections_wide_q4,
          "verify_q4b4": verify_q4b4, "draft": draft, "verify": verify, "attention_30b": attention_30b,
          "lmhead_30b": lmhead_30b, "step_30b_b8": step_30b_b8, "verify_moe": verify_moe}

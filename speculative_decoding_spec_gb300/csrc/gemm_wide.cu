@@ -781,8 +781,10 @@ __global__ void __launch_bounds__(256) wide_prep_kernel(const float* X, int ldx,
   // without a gain, blocks (m, y) split the row's columns (multiples of 8)
   const int per = ((K + gridDim.y - 1) / gridDim.y + 7) / 8 * 8;
   const int kb = blockIdx.y * per, ke = min(K, kb + per);
-  grid_dep_wait();
+  // The projection that follows may start at once: it fetches only weights
+  // until its own wait, which also covers everything this kernel waits for.
   grid_dep_launch();
+  grid_dep_wait();
   uint16_t* hi = xs + (size_t)m * K;
   uint16_t* lo = xs + (size_t)(MP + m) * K;
   if (m >= M) {
