@@ -121,6 +121,21 @@ SPEC_DEV void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* 
       "l"(map), "r"(x), "r"(y), "r"(sa(bar))
       : "memory");
 }
+// With an L2 cache policy: the target's own layers read each layer's pages
+// once per pass, so they go first when L2 needs room (the drafter re-reads the
+// last layer's pages at every step and keeps the default).
+SPEC_DEV void tma_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(sa(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(sa(bar)), "l"(policy)
+      : "memory");
+}
+SPEC_DEV uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 SPEC_DEV void ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
   asm volatile(
@@ -309,30 +324,37 @@ struct Cta {
   SPEC_DEV int row_of(int page, int plane) const { return ((page * 2 + plane) * a.nkv + w.kvh) * PAGE; }
 
   // ---- warp 0, one thread ----
-  SPEC_DEV void load_tile(unsigned char* dst, int blk, int plane, uint64_t* bar) {
+  SPEC_DEV void load_tile(unsigned char* dst, int blk, int plane, uint64_t* bar, bool hint, uint64_t pol) {
     const int p0 = 2 * blk, p1 = min(2 * blk + 1, w.npages - 1);  // a missing second page repeats the first
     const int r0 = row_of(page_id(p0), plane), r1 = row_of(page_id(p1), plane);
     mbar_expect_tx(bar, TILE_BYTES);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      tma_2d(dst + h * HALF_BYTES, tm, 64 * h, r0, bar);
-      tma_2d(dst + h * HALF_BYTES + BOX_BYTES, tm, 64 * h, r1, bar);
+      if (hint) {
+        tma_2d_hint(dst + h * HALF_BYTES, tm, 64 * h, r0, bar, pol);
+        tma_2d_hint(dst + h * HALF_BYTES + BOX_BYTES, tm, 64 * h, r1, bar, pol);
+      } else {
+        tma_2d(dst + h * HALF_BYTES, tm, 64 * h, r0, bar);
+        tma_2d(dst + h * HALF_BYTES + BOX_BYTES, tm, 64 * h, r1, bar);
+      }
     }
   }
   SPEC_DEV void producer() {
     const int nb = nblocks();
+    const bool hint = a.key_extra != 0;  // the target's rows (not the drafter's)
+    const uint64_t pol = l2_evict_first();
     int kn = 0, vn = 0;
     for (int n = 0; n <= nb; ++n) {
       if (n < nb) {
         const int s = n % KSLOTS;
         if (n >= KSLOTS && !wait_phase(&kempty[s], ((n / KSLOTS) - 1) & 1, abort_s, a.err)) break;
-        load_tile(sm + S::K_OFF + (size_t)s * TILE_BYTES, w.blk0 + n, 0, &kfull[s]);
+        load_tile(sm + S::K_OFF + (size_t)s * TILE_BYTES, w.blk0 + n, 0, &kfull[s], hint, pol);
         kn = n + 1;
       }
       if (n >= 1) {
         const int m = n - 1, s = m % VSLOTS;
         if (m >= VSLOTS && !wait_phase(&vempty[s], ((m / VSLOTS) - 1) & 1, abort_s, a.err)) break;
-        load_tile(sm + S::V_OFF + (size_t)s * TILE_BYTES, w.blk0 + m, 1, &vfull[s]);
+        load_tile(sm + S::V_OFF + (size_t)s * TILE_BYTES, w.blk0 + m, 1, &vfull[s], hint, pol);
         vn = m + 1;
       }
     }

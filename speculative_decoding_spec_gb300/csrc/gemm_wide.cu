@@ -143,6 +143,22 @@ SPEC_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint6
       : "memory");
 }
 
+// The same with an L2 cache policy (weights: evict first, so that the stream of
+// bytes read once does not push out the lines that are read again -- the
+// activation planes, the residual rows, the split-tile partials).
+SPEC_DEV void tma_load_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(sa(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(sa(bar)), "l"(policy)
+      : "memory");
+}
+SPEC_DEV uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 // 16 consecutive accumulator columns of this warp's 32 lanes (lane = tile row).
 SPEC_DEV void tmem_ld16(uint32_t taddr, float* v) {
   uint32_t r[16];
@@ -260,26 +276,26 @@ struct Cta {
 
   SPEC_DEV unsigned char* stage(int s) const { return stages + (size_t)s * p.stage_bytes; }
 
-  SPEC_DEV void load_w(int s, int u) const {
+  SPEC_DEV void load_w(int s, int u, uint64_t pol) const {
     const int t = u / p.C, x = (u - t * p.C) * KC;
     if (Q4) {
       // 128 rows x 32 code bytes (64 values); the planes are built from them
       unsigned char* dst = stage(s) + p.c_off;
       if (p.map == MAP_PAIR) {
-        tma_load_2d(dst, tmw, x / 2, t * 64, &full[s]);
-        tma_load_2d(dst + CODE_BYTES / 2, tmw, x / 2, a.geglu_half + t * 64, &full[s]);
+        tma_load_2d_hint(dst, tmw, x / 2, t * 64, &full[s], pol);
+        tma_load_2d_hint(dst + CODE_BYTES / 2, tmw, x / 2, a.geglu_half + t * 64, &full[s], pol);
       } else {
-        tma_load_2d(dst, tmw, x / 2, t * TM, &full[s]);
+        tma_load_2d_hint(dst, tmw, x / 2, t * TM, &full[s], pol);
       }
       return;
     }
     unsigned char* dst = stage(s);
     if (p.map == MAP_PAIR) {
       // rows 0-63: gate rows 64t.., rows 64-127: the matching up rows
-      tma_load_2d(dst, tmw, x, t * 64, &full[s]);
-      tma_load_2d(dst + W_BYTES / 2, tmw, x, a.geglu_half + t * 64, &full[s]);
+      tma_load_2d_hint(dst, tmw, x, t * 64, &full[s], pol);
+      tma_load_2d_hint(dst + W_BYTES / 2, tmw, x, a.geglu_half + t * 64, &full[s], pol);
     } else {
-      tma_load_2d(dst, tmw, x, t * TM, &full[s]);
+      tma_load_2d_hint(dst, tmw, x, t * TM, &full[s], pol);
     }
   }
   SPEC_DEV void load_x(int s, int u) const {
@@ -290,9 +306,10 @@ struct Cta {
   // warp 0, one thread
   SPEC_DEV void producer() {
     const int nu = u1 - u0, pre = min(nu, p.stages);
+    const uint64_t pol = l2_evict_first();
     for (int n = 0; n < pre; ++n) {
       mbar_expect_tx(&full[n], (unsigned)p.tx_bytes);
-      load_w(n, u0 + n);
+      load_w(n, u0 + n, pol);
     }
     grid_dep_wait();  // the activation planes come from the preparation kernel
     stamp(trace, 2);
@@ -302,7 +319,7 @@ struct Cta {
       const int s = n % p.stages;
       if (!wait_phase(&empty[s], ((n / p.stages) - 1) & 1, abort_s, err)) break;
       mbar_expect_tx(&full[s], (unsigned)p.tx_bytes);
-      load_w(s, u0 + n);
+      load_w(s, u0 + n, pol);
       load_x(s, u0 + n);
       issued = n + 1;
     }
