@@ -39,11 +39,19 @@
 // device from the lengths, so the grid is fixed), and the CTAs of a pair
 // write unnormalised partials (O, max, sum), arrive on the pair's counter, wait
 // (bounded) until all have arrived and then each merges a slice of the query
-// rows with log-sum-exp weights. All CTAs of the grid are resident at once
-// (grid <= SMs, one CTA per SM by its shared memory); the launch of the next
-// kernel is triggered only after the wait. A wait that runs out records
-// SPEC_ERR_TIMEOUT and skips the merge; every CTA still departs, and the last
-// to depart resets the pair's counters. Every mbarrier wait is bounded too.
+// rows with log-sum-exp weights. The plan is a warp-wide prefix sum over the
+// pairs; the partials are written CTA-major (32 rows a CTA), one compact block
+// the pair's CTAs read back. All CTAs of the grid are resident at once (grid
+// <= SMs, one CTA per SM by its shared memory), and a dependent kernel is only
+// launched once every CTA of this grid has started, so the wait cannot block
+// on a CTA that never runs. A wait that runs out records SPEC_ERR_TIMEOUT and
+// skips the merge; every CTA still departs, and the last to depart resets the
+// pair's counters. Every mbarrier wait is bounded too.
+//
+// The code after the last block runs once per CTA, out of a cold instruction
+// cache and at the same moment on every SM, so it is kept short: an unrolled
+// loop with per-column index divisions there cost about 8 us a launch, and a
+// serial plan loop with 64-bit divisions another 9 us at 64 pairs.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
@@ -268,7 +276,8 @@ struct Smem {
   static constexpr size_t PG_OFF = L_OFF + 32 * 4;               // int [PGS_CACHE]
   static constexpr size_t ML_OFF = PG_OFF + PGS_CACHE * 4;       // float2 [MERGE_MAX] merge weights
   static constexpr size_t MISC_OFF = ML_OFF + MERGE_MAX * 8;     // int [16]
-  static constexpr size_t BYTES = MISC_OFF + 16 * 4;
+  static constexpr size_t COFF_OFF = MISC_OFF + 16 * 4;          // int [32] output offset of each query column
+  static constexpr size_t BYTES = COFF_OFF + 32 * 4;
   static constexpr size_t ALLOC = BYTES + 1024;                  // base alignment slack
 };
 
@@ -304,6 +313,7 @@ struct Cta {
   unsigned char* sm;
   uint64_t *kfull, *kempty, *vfull, *vempty, *sfull, *pfull, *pvdone, *drain;
   float *red, *mu, *alpha, *lfin;
+  int* coff;                 // [32] offset of query column c's head in `out` (row-major [M][nq*HD])
   int* pgs;
   int* misc;                 // [0] merge ok, [2] tmem base, [3] abort
   volatile int* abort_s;
@@ -424,6 +434,10 @@ struct Cta {
   SPEC_DEV void build_q() {
     const int t = threadIdx.x - SM0;
     const int b = w.b;
+    if (t < p.QN) {
+      const int i = t / p.G, gg = t - i * p.G;
+      coff[t] = (b * a.R + i) * a.nq * HD + (w.kvh * p.G + gg) * HD;
+    }
     for (int u = t; u < 32 * 8; u += NSM) {
       const int q = u >> 3, c8 = u & 7;  // dims 8*c8 .. +7 and 64 + 8*c8 .. +7
       float x0[8], x1[8];
@@ -639,20 +653,23 @@ struct Cta {
 #pragma unroll
       for (int q = 0; q < QG; ++q) o[q] = 0.f;
     }
+    const int nv = min(QG, p.QN - c0);  // this group's columns that are queries
+    if (w.np == 1) {
 #pragma unroll
-    for (int q = 0; q < QG; ++q) {
-      const int c = c0 + q;
-      if (c >= p.QN) break;
-      const int i = c / p.G, gg = c - i * p.G;
-      const int m = w.b * a.R + i, h = w.kvh * p.G + gg;
-      const float lc = lfin[c];
-      if (w.np == 1) {
-        a.out[(size_t)m * a.nq * HD + h * HD + d] = lc > 0.f ? o[q] / lc : 0.f;
-      } else {
-        const size_t pi = ((size_t)m * a.nq + h) * a.max_pages + w.j;
-        __stcg(a.part_o + pi * HD + d, o[q]);
-        if (d == 0) __stcg(reinterpret_cast<float2*>(a.part_ml) + pi, make_float2(mu[c], lc));
-      }
+      for (int q = 0; q < QG; ++q)
+        if (q < nv) {
+          const float lc = lfin[c0 + q];
+          a.out[coff[c0 + q] + d] = lc > 0.f ? o[q] / lc : 0.f;
+        }
+    } else {
+      // partials CTA-major: rows blockIdx.x * 32 + column
+      float* po = a.part_o + ((size_t)blockIdx.x * 32 + c0) * HD + d;
+#pragma unroll
+      for (int q = 0; q < QG; ++q)
+        if (q < nv) __stcg(po + q * HD, o[q]);
+      if (d < nv)
+        __stcg(reinterpret_cast<float2*>(a.part_ml) + (size_t)blockIdx.x * 32 + c0 + d,
+               make_float2(mu[c0 + d], lfin[c0 + d]));
     }
   }
 
@@ -690,13 +707,12 @@ struct Cta {
     const int rows = q1 - q0, n = rows * np;
     const bool go = misc[0] != 0 && n <= MERGE_MAX;
     if (misc[0] && n > MERGE_MAX && t == 0) set_error(a.err, SPEC_ERR_CAPACITY);
-    auto pidx = [&](int k) {
-      const int r = k / np, sp = k - r * np, q = q0 + r;
-      const int i = q / p.G, gg = q - i * p.G;
-      return ((size_t)(w.b * a.R + i) * a.nq + w.kvh * p.G + gg) * a.max_pages + sp;
-    };
+    const size_t first = (size_t)(blockIdx.x - w.j) * 32 + q0;  // row q0 of the pair's first CTA
     if (go)
-      for (int k = t; k < n; k += NSM) ml[k] = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + pidx(k));
+      for (int k = t; k < n; k += NSM) {
+        const int r = k / np, sp = k - r * np;
+        ml[k] = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + first + (size_t)sp * 32 + r);
+      }
     sm_sync();
     if (go && t < rows) {
       float M = -INFINITY, L = 0.f;
@@ -712,25 +728,24 @@ struct Cta {
     }
     sm_sync();
     if (go) {
-      const int ra = (rows * half) / 2, rb = (rows * (half + 1)) / 2;
-      const int ka = ra * np, kb = rb * np;
-      float acc = 0.f;
-      for (int k0 = ka; k0 < kb; k0 += 8) {
-        float u[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) u[e] = k0 + e < kb ? __ldcg(a.part_o + pidx(k0 + e) * HD + d) : 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int k = k0 + e;
-          if (k < kb) {
-            acc = fmaf(ml[k].x, u[e], acc);
-            if ((k + 1) % np == 0) {
-              const int q = q0 + k / np, i = q / p.G, gg = q - i * p.G;
-              a.out[(size_t)(w.b * a.R + i) * a.nq * HD + (w.kvh * p.G + gg) * HD + d] = acc;
-              acc = 0.f;
-            }
-          }
+      // thread = dimension d; the two halves of the threads take alternate
+      // rows; the splits are added in order, four loads in flight
+      constexpr size_t SP = 32 * HD;  // distance between two splits of a row
+      for (int r = half; r < rows; r += 2) {
+        const float* src = a.part_o + (first + r) * HD + d;
+        const float2* wr = ml + r * np;
+        float acc = 0.f;
+        int sp = 0;
+        for (; sp + 4 <= np; sp += 4) {
+          const float u0 = __ldcg(src + sp * SP), u1 = __ldcg(src + (sp + 1) * SP);
+          const float u2 = __ldcg(src + (sp + 2) * SP), u3 = __ldcg(src + (sp + 3) * SP);
+          acc = fmaf(wr[sp].x, u0, acc);
+          acc = fmaf(wr[sp + 1].x, u1, acc);
+          acc = fmaf(wr[sp + 2].x, u2, acc);
+          acc = fmaf(wr[sp + 3].x, u3, acc);
         }
+        for (; sp < np; ++sp) acc = fmaf(wr[sp].x, __ldcg(src + sp * SP), acc);
+        a.out[coff[q0 + r] + d] = acc;
       }
     }
     sm_sync();
@@ -771,7 +786,10 @@ SPEC_DEV bool plan_work(const AttnArgs& a, const Plan& p, int* s_nb, int* misc, 
     __syncthreads();
     return pr < p.npairs;
   }
-  if (tid == 0) s_tot = 0;
+  if (tid == 0) {
+    s_tot = 0;
+    s_pair = -1;
+  }
   __syncthreads();
   for (int pr = tid; pr < p.npairs; pr += blockDim.x) {
     const int b = pr / a.nkv;
@@ -786,23 +804,34 @@ SPEC_DEV bool plan_work(const AttnArgs& a, const Plan& p, int* s_nb, int* misc, 
     atomicAdd(&s_tot, s_nb[pr]);
   }
   __syncthreads();
-  if (tid == 0) {
-    const int extra = p.grid - p.npairs;
-    const int tot = s_tot;
-    int c0 = 0;
-    s_pair = -1;
-    for (int pr = 0; pr < p.npairs; ++pr) {
-      const int nb = s_nb[pr];
-      int np = 1;
-      if (extra > 0 && tot > 0) np += (int)(((long long)extra * nb) / tot);
-      np = min(np, max(nb, 1));
-      if ((int)blockIdx.x >= c0 && (int)blockIdx.x < c0 + np) {
+  if (tid < 32) {
+    // warp 0: each pair's CTA count, and an exclusive prefix sum over the
+    // pairs (32 at a time) that places this CTA
+    const int extra = p.grid - p.npairs, tot = s_tot;
+    int run = 0;
+    for (int base = 0; base < p.npairs; base += 32) {
+      const int pr = base + tid;
+      int nb = 0, np = 0;
+      if (pr < p.npairs) {
+        nb = s_nb[pr];
+        np = 1;
+        if (extra > 0 && tot > 0) np += (int)(((long long)extra * nb) / tot);
+        np = min(np, max(nb, 1));
+      }
+      int incl = np;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += v;
+      }
+      const int c0 = run + incl - np;
+      if (np > 0 && (int)blockIdx.x >= c0 && (int)blockIdx.x < c0 + np) {
         s_pair = pr;
         s_j = (int)blockIdx.x - c0;
         s_np = np;
         s_nbp = nb;
       }
-      c0 += np;
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
   __syncthreads();
@@ -844,6 +873,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   k.mu = reinterpret_cast<float*>(sm + S::MU_OFF);
   k.alpha = reinterpret_cast<float*>(sm + S::AL_OFF);
   k.lfin = reinterpret_cast<float*>(sm + S::L_OFF);
+  k.coff = reinterpret_cast<int*>(sm + S::COFF_OFF);
   k.pgs = reinterpret_cast<int*>(sm + S::PG_OFF);
   k.misc = reinterpret_cast<int*>(sm + S::MISC_OFF);
   k.abort_s = reinterpret_cast<volatile int*>(k.misc + 3);
@@ -902,6 +932,9 @@ __global__ void __launch_bounds__(NTHR, 1)
   fence_before();
   __syncthreads();
   fence_after();
+  // every CTA of this grid is resident past this point: the next kernel may be
+  // scheduled (it waits for this grid's completion before reading its output)
+  grid_dep_launch();
 
   if (have) {
     if (warp == 0) {
@@ -927,7 +960,6 @@ __global__ void __launch_bounds__(NTHR, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(k.tmem), "r"(TMEM_COLS) : "memory");
   }
   if (have && k.w.np > 1 && warp >= 2) k.merge(!aborted);
-  grid_dep_launch();
 }
 
 template <int QNP>
@@ -983,6 +1015,8 @@ int attention_flash(const AttnArgs& a, unsigned int* counters, int wait_extra, c
   Plan p;
   p.npairs = a.B * a.nkv;
   p.grid = std::max(p.npairs, std::min(num_sms(), p.npairs * std::max(1, (a.max_pages + 1) / 2)));
+  // split CTAs write their partials CTA-major (32 rows each)
+  if (p.grid > p.npairs && (size_t)p.grid * 32 > (size_t)ATTN_FLASH_PART_ROWS) return -2;
   p.R = a.R;
   p.G = a.nq / a.nkv;
   p.QN = a.R * p.G;

@@ -313,6 +313,11 @@ size_t attention_smem(int hd, int qn);
 // bounded wait run out (failure-detection tests only). Returns 1, -2 when the
 // shape is not covered, -1 on a launch error.
 void setup_attn_flash_attributes();
+// The tcgen05 attention's partials are CTA-major: CTA c writes query rows
+// [c*32, c*32 + 32) of part_o / part_ml (a compact block the pair's CTAs read
+// back), so the partial buffers hold at least this many rows on top of the
+// pair-major layout of the other attention kernels.
+constexpr int ATTN_FLASH_PART_ROWS = 256 * 32;
 bool attention_flash_ok(const AttnArgs& a);
 int attention_flash(const AttnArgs& a, unsigned int* counters, int wait_extra, cudaStream_t st);
 

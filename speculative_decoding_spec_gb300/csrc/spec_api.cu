@@ -83,8 +83,8 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
   w.qkv = b.take<float>(base, M * nqkv);
   w.att = b.take<float>(base, M * qd);
   w.act = b.take<float>(base, M * m.d_ff);
-  w.part_o = b.take<float>(base, M * m.n_q_heads * (size_t)max_pages * m.head_dim);
-  w.part_ml = b.take<float>(base, M * m.n_q_heads * (size_t)max_pages * 2);
+  w.part_o = b.take<float>(base, (M * m.n_q_heads * (size_t)max_pages + ATTN_FLASH_PART_ROWS) * m.head_dim);
+  w.part_ml = b.take<float>(base, (M * m.n_q_heads * (size_t)max_pages + ATTN_FLASH_PART_ROWS) * 2);
   w.rope_cs = b.take<float>(base, M * m.head_dim);
   w.pos = b.take<int32_t>(base, M);
   w.sel_row = b.take<int32_t>(base, B_max);
@@ -138,8 +138,8 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
     w.d_h = b.take<float>(base, (size_t)B_max * m.d_model);
     w.d_scores = b.take<float>(base, (size_t)B_max * std::max(d->n_centroids, 1));
     w.d_rope = b.take<float>(base, (size_t)B_max * m.head_dim);
-    w.d_part_o = b.take<float>(base, (size_t)B_max * d->n_q_heads * max_pages * m.head_dim);
-    w.d_part_ml = b.take<float>(base, (size_t)B_max * d->n_q_heads * max_pages * 2);
+    w.d_part_o = b.take<float>(base, ((size_t)B_max * d->n_q_heads * max_pages + ATTN_FLASH_PART_ROWS) * m.head_dim);
+    w.d_part_ml = b.take<float>(base, ((size_t)B_max * d->n_q_heads * max_pages + ATTN_FLASH_PART_ROWS) * 2);
     w.d_chosen = b.take<int32_t>(base, (size_t)B_max * std::max(d->top_c, 1));
     w.d_drafts = b.take<int32_t>(base, (size_t)B_max * KMAX);
     w.d_best = b.take<unsigned long long>(base, B_max);
@@ -270,8 +270,8 @@ AttnWork carve_attention(char* base, int B, int R, int nq, int nkv, int hd, int 
   const size_t M = (size_t)B * R;
   w.err = b.take<int>(base, 4);
   w.counters = b.take<unsigned int>(base, (size_t)2 * B * nkv);
-  w.part_o = b.take<float>(base, M * nq * (size_t)max_pages * hd);
-  w.part_ml = b.take<float>(base, M * nq * (size_t)max_pages * 2);
+  w.part_o = b.take<float>(base, (M * nq * (size_t)max_pages + ATTN_FLASH_PART_ROWS) * hd);
+  w.part_ml = b.take<float>(base, (M * nq * (size_t)max_pages + ATTN_FLASH_PART_ROWS) * 2);
   w.bytes = (b.off + 255) & ~size_t(255);
   return w;
 }
