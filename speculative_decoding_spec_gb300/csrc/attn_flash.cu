@@ -320,6 +320,7 @@ struct Cta {
   uint32_t tmem;
   Work w;
   int slot, L0;
+  int kpre, vpre;  // K and V blocks the producer issued before the dependency wait
 
   SPEC_DEV int nblocks() const { return w.blk1 - w.blk0; }
   SPEC_DEV int page_id(int pidx) const {
@@ -349,19 +350,38 @@ struct Cta {
       }
     }
   }
+  // Before the dependency wait: the first ring slots for blocks whose keys are
+  // all committed positions (below seq_len), which the previous kernels of
+  // this pass do not write. The drafter's keys are all committed.
+  SPEC_DEV void preissue() {
+    const int nb = nblocks();
+    const bool hint = a.key_extra != 0;
+    const uint64_t pol = l2_evict_first();
+    auto safe = [&](int n) { return a.key_extra == 0 || BK * (w.blk0 + n + 1) <= L0; };
+    kpre = 0;
+    vpre = 0;
+    while (kpre < min(KSLOTS, nb) && safe(kpre)) {
+      load_tile(sm + S::K_OFF + (size_t)kpre * TILE_BYTES, w.blk0 + kpre, 0, &kfull[kpre], hint, pol);
+      ++kpre;
+    }
+    while (vpre < min(VSLOTS, nb) && safe(vpre)) {
+      load_tile(sm + S::V_OFF + (size_t)vpre * TILE_BYTES, w.blk0 + vpre, 1, &vfull[vpre], hint, pol);
+      ++vpre;
+    }
+  }
   SPEC_DEV void producer() {
     const int nb = nblocks();
     const bool hint = a.key_extra != 0;  // the target's rows (not the drafter's)
     const uint64_t pol = l2_evict_first();
-    int kn = 0, vn = 0;
+    int kn = kpre, vn = vpre;
     for (int n = 0; n <= nb; ++n) {
-      if (n < nb) {
+      if (n < nb && n >= kpre) {
         const int s = n % KSLOTS;
         if (n >= KSLOTS && !wait_phase(&kempty[s], ((n / KSLOTS) - 1) & 1, abort_s, a.err)) break;
         load_tile(sm + S::K_OFF + (size_t)s * TILE_BYTES, w.blk0 + n, 0, &kfull[s], hint, pol);
         kn = n + 1;
       }
-      if (n >= 1) {
+      if (n >= 1 && n - 1 >= vpre) {
         const int m = n - 1, s = m % VSLOTS;
         if (m >= VSLOTS && !wait_phase(&vempty[s], ((m / VSLOTS) - 1) & 1, abort_s, a.err)) break;
         load_tile(sm + S::V_OFF + (size_t)s * TILE_BYTES, w.blk0 + m, 1, &vfull[s], hint, pol);
@@ -729,23 +749,37 @@ struct Cta {
     sm_sync();
     if (go) {
       // thread = dimension d; the two halves of the threads take alternate
-      // rows; the splits are added in order, four loads in flight
+      // rows, two rows at a time; each row's splits are added in order, with
+      // up to eight loads in flight
       constexpr size_t SP = 32 * HD;  // distance between two splits of a row
-      for (int r = half; r < rows; r += 2) {
-        const float* src = a.part_o + (first + r) * HD + d;
-        const float2* wr = ml + r * np;
-        float acc = 0.f;
+      for (int r = half; r < rows; r += 4) {
+        const bool two = r + 2 < rows;
+        const float* s0 = a.part_o + (first + r) * HD + d;
+        const float* s1 = two ? s0 + 2 * HD : s0;
+        const float2* w0 = ml + r * np;
+        const float2* w1 = two ? w0 + 2 * np : w0;
+        float acc0 = 0.f, acc1 = 0.f;
         int sp = 0;
         for (; sp + 4 <= np; sp += 4) {
-          const float u0 = __ldcg(src + sp * SP), u1 = __ldcg(src + (sp + 1) * SP);
-          const float u2 = __ldcg(src + (sp + 2) * SP), u3 = __ldcg(src + (sp + 3) * SP);
-          acc = fmaf(wr[sp].x, u0, acc);
-          acc = fmaf(wr[sp + 1].x, u1, acc);
-          acc = fmaf(wr[sp + 2].x, u2, acc);
-          acc = fmaf(wr[sp + 3].x, u3, acc);
+          float u[4], v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            u[i] = __ldcg(s0 + (sp + i) * SP);
+            v[i] = __ldcg(s1 + (sp + i) * SP);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc0 = fmaf(w0[sp + i].x, u[i], acc0);
+            acc1 = fmaf(w1[sp + i].x, v[i], acc1);
+          }
         }
-        for (; sp < np; ++sp) acc = fmaf(wr[sp].x, __ldcg(src + sp * SP), acc);
-        a.out[coff[q0 + r] + d] = acc;
+        for (; sp < np; ++sp) {
+          const float u = __ldcg(s0 + sp * SP), v = __ldcg(s1 + sp * SP);
+          acc0 = fmaf(w0[sp].x, u, acc0);
+          acc1 = fmaf(w1[sp].x, v, acc1);
+        }
+        a.out[coff[q0 + r] + d] = acc0;
+        if (two) a.out[coff[q0 + r + 2] + d] = acc1;
       }
     }
     sm_sync();
@@ -906,14 +940,17 @@ __global__ void __launch_bounds__(NTHR, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // everything below reads the previous kernel's outputs (queries, new keys
-  // and values, lengths)
-  grid_dep_wait();
+  // The lengths, sequence ids and page tables are not written by the kernels
+  // of a pass (the previous pass's commit wrote the lengths, and every earlier
+  // kernel had completed before the one just before this launched it), so the
+  // plan, the page ids and the first committed blocks come before the wait;
+  // the queries and the pass's new keys and values come after it.
   const bool have = plan_work(a, p, s_nb, k.misc, k.w);  // contains __syncthreads
   fence_before();
   __syncthreads();
   fence_after();
   k.tmem = *reinterpret_cast<uint32_t*>(k.misc + 2);
+  k.kpre = k.vpre = 0;
   if (have) {
     k.slot = a.seq_ids[k.w.b];
     k.L0 = a.seq_len[k.slot];
@@ -927,8 +964,11 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
       k.pgs[pi - pa] = pg;
     }
-    if (warp >= 2) k.build_q();
   }
+  __syncthreads();
+  if (have && threadIdx.x == 0) k.preissue();
+  grid_dep_wait();
+  if (have && warp >= 2) k.build_q();
   fence_before();
   __syncthreads();
   fence_after();
@@ -1033,7 +1073,7 @@ int attention_flash(const AttnArgs& a, unsigned int* counters, int wait_extra, c
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.standalone ? 0 : 1;
   cudaError_t e;
   if (p.QN <= 8) {
     cfg.dynamicSmemBytes = Smem::ALLOC;

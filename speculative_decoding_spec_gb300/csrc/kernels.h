@@ -170,6 +170,7 @@ struct AttnArgs {
   float* part_ml;           // [M][nq][n_split][2]
   float* out;               // [M][nq*hd] merged output
   int* err;
+  int standalone;           // 1: launched outside the library's kernel chain (no programmatic launch)
 };
 int attention(const AttnArgs& a, cudaStream_t st);
 

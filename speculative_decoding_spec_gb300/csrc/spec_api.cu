@@ -809,7 +809,7 @@ spec_status spec_attention(const spec_model_desc* m, const spec_kv_desc* kv, int
   at.layer = layer; at.n_pages = kv->n_pages; at.max_pages = kv->max_pages_per_seq;
   at.block_table = kv->block_table; at.seq_ids = seq_ids; at.seq_len = seq_len; at.rope_cs = nullptr;
   at.n_split = kv->max_pages_per_seq; at.pages_per_split = 1; at.part_o = w.part_o; at.part_ml = w.part_ml;
-  at.out = out; at.err = w.err;
+  at.out = out; at.err = w.err; at.standalone = 1;
   setup_device_attributes();
   if (launch_attention(m->kv_dtype, at, w.counters, 0, (cudaStream_t)stream) < 0) return SPEC_ECUDA;
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
