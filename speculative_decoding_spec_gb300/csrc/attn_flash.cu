@@ -323,6 +323,22 @@ struct Cta {
   int kpre, vpre;  // K and V blocks the producer issued before the dependency wait
 
   SPEC_DEV int nblocks() const { return w.blk1 - w.blk0; }
+  // A merged output value (offset `at` in out [M][nq*HD]), and the same as
+  // the hi + lo activation planes of the projection that follows.
+  SPEC_DEV void put_out(size_t at, float v) const {
+    a.out[at] = v;
+    if (!a.planes) return;
+    const size_t lo = at + (size_t)a.planes_mp * a.nq * HD;
+    if (a.planes_f16) {
+      const __half h = __float2half_rn(v), l = __float2half_rn(v - __half2float(h));
+      a.planes[at] = __half_as_ushort(h);
+      a.planes[lo] = __half_as_ushort(l);
+    } else {
+      const __nv_bfloat16 h = __float2bfloat16_rn(v), l = __float2bfloat16_rn(v - __bfloat162float(h));
+      a.planes[at] = __bfloat16_as_ushort(h);
+      a.planes[lo] = __bfloat16_as_ushort(l);
+    }
+  }
   SPEC_DEV int page_id(int pidx) const {
     const int local = pidx - 2 * w.blk0;
     if (local >= 0 && local < PGS_CACHE) return pgs[local];
@@ -679,7 +695,7 @@ struct Cta {
       for (int q = 0; q < QG; ++q)
         if (q < nv) {
           const float lc = lfin[c0 + q];
-          a.out[coff[c0 + q] + d] = lc > 0.f ? o[q] / lc : 0.f;
+          put_out((size_t)coff[c0 + q] + d, lc > 0.f ? o[q] / lc : 0.f);
         }
     } else {
       // partials CTA-major: rows blockIdx.x * 32 + column
@@ -778,8 +794,8 @@ struct Cta {
           acc0 = fmaf(w0[sp].x, u, acc0);
           acc1 = fmaf(w1[sp].x, v, acc1);
         }
-        a.out[coff[q0 + r] + d] = acc0;
-        if (two) a.out[coff[q0 + r + 2] + d] = acc1;
+        put_out((size_t)coff[q0 + r] + d, acc0);
+        if (two) put_out((size_t)coff[q0 + r + 2] + d, acc1);
       }
     }
     sm_sync();

@@ -249,6 +249,20 @@ struct SegIter {
   }
 };
 
+// v as hi + lo halves (hi = v rounded, lo = the rest rounded), the split the
+// preparation kernel makes, stored at xs[hi_at] and xs[lo_at].
+SPEC_DEV void put_planes(uint16_t* xs, size_t hi_at, size_t lo_at, float v, int f16) {
+  if (f16) {
+    const __half h = __float2half_rn(v), l = __float2half_rn(v - __half2float(h));
+    xs[hi_at] = __half_as_ushort(h);
+    xs[lo_at] = __half_as_ushort(l);
+  } else {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v), l = __float2bfloat16_rn(v - __bfloat162float(h));
+    xs[hi_at] = __bfloat16_as_ushort(h);
+    xs[lo_at] = __bfloat16_as_ushort(l);
+  }
+}
+
 // ---- one CTA ----------------------------------------------------------------
 
 template <int MP, bool Q4>
@@ -456,7 +470,7 @@ struct Cta {
   // compact (it runs once per tile, with a cold instruction cache) and every
   // thread can take any (row, column) of the tile.
   SPEC_DEV void finish(int t, const float (&v)[MP], unsigned long long& mybest) {
-    const int r = row(), e = threadIdx.x - EPI0;
+    const int r = row();
 #pragma unroll
     for (int m = 0; m < MP; ++m) xch[m * XCH_LD + r] = v[m] * rms_s[m];
     epi_sync();
@@ -540,7 +554,11 @@ struct Cta {
     for (int m = ma + (e >> 6); m < mb; m += 2) {
       const float g = xch[m * XCH_LD + c];
       const float gl = 0.5f * g * (1.f + erff(g * 0.70710678118654752f));
-      a.Y[(size_t)m * a.ldy + j] = gl * xch[m * XCH_LD + 64 + c];
+      const float v = gl * xch[m * XCH_LD + 64 + c];
+      a.Y[(size_t)m * a.ldy + j] = v;
+      if (a.wide.out_xs)
+        put_planes(a.wide.out_xs, (size_t)m * a.geglu_half + j, (size_t)(MP + m) * a.geglu_half + j, v,
+                   a.wide.out_f16);
     }
   }
 
@@ -636,7 +654,11 @@ struct Cta {
     const int e = threadIdx.x - EPI0;
     grid_dep_wait();
     grid_dep_launch();
-    if (e < 64) rms_s[e] = e < a.M ? __ldcg(inv_rms + e) : 0.f;
+    if (e < 64) {
+      // 1/rms of each row from the preparation kernel; planes written by the
+      // producer are never normalised
+      rms_s[e] = e < a.M ? (a.wide.ready ? 1.f : __ldcg(inv_rms + e)) : 0.f;
+    }
     if (p.map == MAP_ROPE) load_rope_tables();
     if (a.epi == EPI_ADD) {
       // the residual rows of this CTA's tiles towards L2 while the weights
@@ -1047,8 +1069,8 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
   pc.stream = st;
   pc.attrs = attr;
   pc.numAttrs = a.pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&pc, wide_prep_kernel, a.X, a.ldx, a.M, a.K, a.gain, a.eps, p.MP, a.wide.xs, a.wide.rms,
-                         p.q4) != cudaSuccess)
+  if (!a.wide.ready && cudaLaunchKernelEx(&pc, wide_prep_kernel, a.X, a.ldx, a.M, a.K, a.gain, a.eps, p.MP,
+                                          a.wide.xs, a.wide.rms, p.q4) != cudaSuccess)
     return -1;
   cudaLaunchConfig_t cfg = pc;
   cfg.gridDim = dim3(p.grid);
@@ -1069,7 +1091,7 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
     case 48: e = launch_mp<48>(cfg, a, p, tmw, tmx); break;
     default: e = launch_mp<64>(cfg, a, p, tmw, tmx); break;
   }
-  return e == cudaSuccess ? 2 : -1;
+  return e == cudaSuccess ? (a.wide.ready ? 1 : 2) : -1;
 }
 
 }  // namespace spec

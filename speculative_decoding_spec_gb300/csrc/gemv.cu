@@ -480,12 +480,16 @@ void setup_gemv_attributes() {
 // kernel (each streams W again). The choice for a matrix does not depend on
 // the row count when the matrix is large, so a one-row decode and a k+1-row
 // verify of it run the same kernel.
-int gemv(const GemvArgs& a0, cudaStream_t st) {
-  int launched = 0;
+bool gemv_goes_wide(const GemvArgs& a0) {
   GemvArgs first = a0;
   first.M = std::min(64, a0.M);
   const bool large = a0.W.dtype == DT_BF16 && (long long)a0.N * a0.K >= WIDE_MIN_ELEMS && a0.K >= WIDE_MIN_K;
-  const bool wide = (a0.M > 8 || large) && gemv_wide_ok(first);
+  return (a0.M > 8 || large) && gemv_wide_ok(first);
+}
+
+int gemv(const GemvArgs& a0, cudaStream_t st) {
+  int launched = 0;
+  const bool wide = gemv_goes_wide(a0);
   const int step = wide ? 64 : 8;
   for (int m0 = 0; m0 < a0.M; m0 += step) {
     GemvArgs a = a0;

@@ -90,6 +90,15 @@ struct WideScratch {
   int kmax;                 // largest K the planes hold
   int* err;                 // device error word (timeouts), may be null
   unsigned long long* trace;  // optional [grid][16] globaltimer stamps of this launch
+  // Planes written by the kernel that produced this launch's input, with no
+  // RMSNorm on it (the attention before O, the gated GELU before down):
+  // `ready` = 1, no preparation kernel, 1/rms = 1.
+  int ready;
+  // This launch's EPI_GEGLU output as the next projection's planes:
+  // out_xs [2][MP][N'] (N' = the output width), fp16 when out_f16 (a Q4_0
+  // consumer), or null.
+  uint16_t* out_xs;
+  int out_f16;
 };
 
 struct GemvArgs {
@@ -114,6 +123,9 @@ struct GemvArgs {
   unsigned long long* tc_trace;  // optional [grid][16] globaltimer stamps of a register-fragment launch
 };
 int gemv(const GemvArgs& a, cudaStream_t st);
+// True when gemv() runs this projection on the tcgen05 kernel (one launch
+// for up to 64 rows).
+bool gemv_goes_wide(const GemvArgs& a);
 
 // Per-pass row setup: tokens, positions and RoPE cos/sin for M = B*R rows.
 struct RowsArgs {
@@ -171,6 +183,11 @@ struct AttnArgs {
   float* out;               // [M][nq*hd] merged output
   int* err;
   int standalone;           // 1: launched outside the library's kernel chain (no programmatic launch)
+  // tcgen05 kernel only: the merged rows also as the next projection's
+  // activation planes, hi at planes[m][c], lo at planes[planes_mp + m][c]
+  // (c < nq*hd; fp16 when planes_f16), or null
+  uint16_t* planes;
+  int planes_mp, planes_f16;
 };
 int attention(const AttnArgs& a, cudaStream_t st);
 

@@ -43,6 +43,7 @@ struct Work {
   float* tc_fix;
   unsigned int* tc_cnt;
   WideScratch wide;         // tcgen05 projection scratch (null when passes have <= 8 rows)
+  uint16_t* xs_alt;         // second activation-plane buffer (planes written by a producer kernel)
   int* err;
   // drafter
   float *d_cat, *d_u, *d_q, *d_att, *d_act, *d_h, *d_scores, *d_rope, *d_part_o, *d_part_ml;
@@ -127,6 +128,7 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
     w.wide.rms = b.take<float>(base, 64);
     w.wide.fix = b.take<float>(base, gemv_wide_fix_bytes() / sizeof(float));
     w.wide.err = w.err;
+    w.xs_alt = b.take<uint16_t>(base, gemv_wide_xs_bytes(kmax) / 2);
   }
   if (d) {
     const int dq = d->n_q_heads * m.head_dim;
@@ -212,15 +214,32 @@ struct spec_ctx {
 
 namespace {
 
-int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st);
+// Where a tcgen05 projection takes its activation planes from, and whether it
+// writes the next projection's planes (see enqueue_pass).
+struct PlaneCfg {
+  uint16_t* in_xs = nullptr;
+  int ready = 0;
+  uint16_t* out_xs = nullptr;
+  int out_f16 = 0;
+};
+int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st, const PlaneCfg* pc = nullptr);
 
 int kv_dt(const spec_ctx* c) { return c->m.kv_dtype == SPEC_F32 ? DT_F32 : DT_BF16; }
 
 // Tensor-core attention for bf16 caches with head_dim 64/128; the CUDA-core
 // kernels otherwise (fp32 caches). `counters` [B][nkv] are zero between
 // launches; the partial buffers of `at` hold max_pages splits per row and head.
-int launch_attention(int kv_dtype, AttnArgs at, unsigned int* counters, int wait_extra, cudaStream_t st) {
-  if (kv_dtype == SPEC_BF16 && attention_flash_ok(at)) return attention_flash(at, counters, wait_extra, st);
+int launch_attention(int kv_dtype, AttnArgs at, unsigned int* counters, int wait_extra, cudaStream_t st,
+                     bool* flash = nullptr) {
+  if (flash) *flash = false;
+  if (kv_dtype == SPEC_BF16 && attention_flash_ok(at)) {
+    const int r = attention_flash(at, counters, wait_extra, st);
+    if (r != -2) {
+      if (flash) *flash = r > 0;
+      return r;
+    }
+  }
+  at.planes = nullptr;  // only the tcgen05 kernel writes planes
   if (kv_dtype == SPEC_BF16 && (at.hd == 64 || at.hd == 128)) {
     int pps = 1;
     at.n_split = attention_tc_splits(at.B, at.nkv, at.max_pages, &pps, at.R * (at.nq / at.nkv));
@@ -233,8 +252,8 @@ int launch_attention(int kv_dtype, AttnArgs at, unsigned int* counters, int wait
   return attention(at, st);
 }
 
-int run_attention(spec_ctx* c, AttnArgs at, cudaStream_t st) {
-  return launch_attention(c->m.kv_dtype, at, c->wk.attn_count, c->test_attn_wait, st);
+int run_attention(spec_ctx* c, AttnArgs at, cudaStream_t st, bool* flash = nullptr) {
+  return launch_attention(c->m.kv_dtype, at, c->wk.attn_count, c->test_attn_wait, st, flash);
 }
 
 }  // namespace
@@ -300,13 +319,82 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
   ra.parents = parents; ra.tree_mask = parents ? w.tmask : nullptr;
   LAUNCH(embed_rows(ra, st));
 
-  const bool fused_rope = c->fused_rope;
-  for (int l = 0; l < m.n_layers; ++l) {
+  // Activation planes written by the producer. Where the tcgen05 attention
+  // feeds O, or a tcgen05 gate/up projection feeds down, the producer also
+  // writes the consumer's bf16 (fp16 for Q4_0) hi + lo planes into the plane
+  // buffer it does not read itself, and the consumer has no preparation
+  // kernel. (These links have no RMSNorm; folding the norm into a residual
+  // add's epilogue cost that epilogue about as much as it saved.) The two
+  // buffers alternate; a producer writes after its dependency wait, when
+  // every earlier reader has finished.
+  const bool fuse = w.wide.xs && w.xs_alt && M <= 64;
+  uint16_t* bufs[2] = {w.wide.xs, w.xs_alt};
+  const int f16 = m.w_dtype == SPEC_Q4_0 ? 1 : 0;
+  int rd = -1;          // buffer holding the next projection's planes
+  int in_idx = 0;       // buffer the latest tcgen05 projection read
+  auto wide_of = [&](const GemvArgs& g) {
+    GemvArgs t = g;
+    t.wide = w.wide;
+    t.tc_cnt = w.tc_cnt;
+    return fuse && gemv_goes_wide(t);
+  };
+  // consumer side of projection g (wide: g runs on the tcgen05 kernel)
+  auto take = [&](PlaneCfg& pc, bool wide) {
+    if (wide && rd >= 0) {
+      pc.in_xs = bufs[rd];
+      pc.ready = 1;
+      in_idx = rd;
+    } else if (wide) {
+      pc.in_xs = bufs[0];
+      in_idx = 0;
+    }
+    rd = -1;
+  };
+  // the projections after the attention, built ahead so that their routes are known
+  auto o_args = [&](int l) {
+    GemvArgs g = {};
+    g.X = w.att; g.ldx = qd; g.M = M; g.N = d; g.K = qd;
+    g.W = mat_layer(M_(c->w.wo), l, d, qd);
+    g.epi = EPI_ADD; g.Y = w.x; g.ldy = d; g.pdl = 1;
+    return g;
+  };
+  auto gu_args = [&](int l) {
+    GemvArgs g = {};
+    g.X = w.x; g.ldx = d; g.M = M; g.N = 2 * ff; g.K = d;
+    g.W = mat_layer(M_(c->w.wgu), l, 2 * ff, d);
+    g.gain = c->w.g_ffn + (size_t)l * d; g.eps = m.rms_eps;
+    g.epi = EPI_GEGLU; g.geglu_half = ff; g.Y = w.act; g.ldy = ff; g.pdl = 1;
+    return g;
+  };
+  auto down_args = [&](int l) {
+    GemvArgs g = {};
+    g.X = w.act; g.ldx = ff; g.M = M; g.N = d; g.K = ff;
+    g.W = mat_layer(M_(c->w.wdown), l, d, ff);
+    g.epi = EPI_ADD; g.Y = w.x; g.ldy = d; g.pdl = 1;
+    return g;
+  };
+  auto qkv_args = [&](int l) {
     GemvArgs g = {};
     g.X = w.x; g.ldx = d; g.M = M; g.N = nqkv; g.K = d;
     g.W = mat_layer(M_(c->w.wqkv), l, nqkv, d);
     g.gain = c->w.g_attn + (size_t)l * d; g.eps = m.rms_eps;
     g.epi = EPI_STORE; g.Y = w.qkv; g.ldy = nqkv; g.pdl = 1;
+    return g;
+  };
+  auto head_args = [&]() {
+    GemvArgs g = {};
+    g.X = w.x; g.ldx = d; g.M = M; g.N = m.vocab; g.K = d;
+    g.W = M_(c->w.embed);
+    g.gain = c->w.g_final; g.eps = m.rms_eps;
+    g.epi = EPI_ARGMAX; g.Y = logits; g.ldy = m.vocab; g.best = w.best; g.pdl = 1;
+    return g;
+  };
+
+  const bool fused_rope = c->fused_rope;
+  for (int l = 0; l < m.n_layers; ++l) {
+    GemvArgs g = qkv_args(l);
+    PlaneCfg pq;
+    take(pq, wide_of(g));
     if (fused_rope) {
       g.epi = EPI_ROPE;
       RopeEpi& e = g.rope;
@@ -314,7 +402,7 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
       e.pool = c->kv.pool; e.layer_off = (long long)l * c->layer_elems; e.n_pages = c->kv.n_pages;
       e.max_pages = c->kv.max_pages_per_seq; e.block_table = c->kv.block_table; e.err = w.err;
     }
-    LAUNCH(run_gemv(c, g, st));
+    LAUNCH(run_gemv(c, g, st, &pq));
 
     if (!fused_rope) {
     RopeAppendArgs rp = {};
@@ -333,13 +421,20 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     at.rope_cs = nullptr; at.n_split = c->kv.max_pages_per_seq; at.pages_per_split = 1;
     at.part_o = w.part_o; at.part_ml = w.part_ml; at.out = w.att; at.err = w.err;
     at.tree_mask = parents ? w.tmask : nullptr;
-    LAUNCH(run_attention(c, at, st));
+    g = o_args(l);
+    const bool o_wide = wide_of(g);
+    if (o_wide) {
+      at.planes = bufs[1 - in_idx];
+      at.planes_mp = (M + 15) / 16 * 16;
+      at.planes_f16 = f16;
+    }
+    bool flash = false;
+    LAUNCH(run_attention(c, at, st, &flash));
+    if (o_wide && flash) rd = 1 - in_idx;
 
-    g = GemvArgs{};
-    g.X = w.att; g.ldx = qd; g.M = M; g.N = d; g.K = qd;
-    g.W = mat_layer(M_(c->w.wo), l, d, qd);
-    g.epi = EPI_ADD; g.Y = w.x; g.ldy = d; g.pdl = 1;
-    LAUNCH(run_gemv(c, g, st));
+    PlaneCfg po;
+    take(po, o_wide);
+    LAUNCH(run_gemv(c, g, st, &po));
 
     if (m.n_experts > 0) {
       // mixture of experts: normalised rows, router scores, routing, grouped
@@ -358,25 +453,27 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
       LAUNCH(moe_ffn(ma, gu.data, dn.data, m.w_dtype == SPEC_F32 ? DT_F32 : DT_BF16, st));
       continue;
     }
-    g = GemvArgs{};
-    g.X = w.x; g.ldx = d; g.M = M; g.N = 2 * ff; g.K = d;
-    g.W = mat_layer(M_(c->w.wgu), l, 2 * ff, d);
-    g.gain = c->w.g_ffn + (size_t)l * d; g.eps = m.rms_eps;
-    g.epi = EPI_GEGLU; g.geglu_half = ff; g.Y = w.act; g.ldy = ff; g.pdl = 1;
-    LAUNCH(run_gemv(c, g, st));
+    g = gu_args(l);
+    const bool gu_wide = wide_of(g);
+    PlaneCfg pg;
+    take(pg, gu_wide);
+    const GemvArgs gd = down_args(l);
+    const bool dn_wide = wide_of(gd);
+    if (gu_wide && dn_wide) {
+      pg.out_xs = bufs[1 - in_idx];
+      pg.out_f16 = f16;
+    }
+    LAUNCH(run_gemv(c, g, st, &pg));
+    if (pg.out_xs) rd = 1 - in_idx;
 
-    g = GemvArgs{};
-    g.X = w.act; g.ldx = ff; g.M = M; g.N = d; g.K = ff;
-    g.W = mat_layer(M_(c->w.wdown), l, d, ff);
-    g.epi = EPI_ADD; g.Y = w.x; g.ldy = d; g.pdl = 1;
-    LAUNCH(run_gemv(c, g, st));
+    PlaneCfg pd;
+    take(pd, dn_wide);
+    LAUNCH(run_gemv(c, gd, st, &pd));
   }
 
-  GemvArgs g = {};
-  g.X = w.x; g.ldx = d; g.M = M; g.N = m.vocab; g.K = d;
-  g.W = M_(c->w.embed);
-  g.gain = c->w.g_final; g.eps = m.rms_eps;
-  g.epi = EPI_ARGMAX; g.Y = logits; g.ldy = m.vocab; g.best = w.best; g.pdl = 1;
+  GemvArgs g = head_args();
+  PlaneCfg ph;
+  take(ph, wide_of(g));
   TailArgs& t = g.tail;
   t.mode = mode; t.B = B; t.R = R; t.k = R - 1; t.seq_ids = seq_ids; t.drafts = tokens;
   t.out_tokens = out_tokens; t.n_emitted = n_emitted; t.seq_len = c->state.seq_len;
@@ -393,7 +490,7 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     if (!g.Y) g.Y = w.lg;
     t.mode = TAIL_NONE;
   }
-  LAUNCH(run_gemv(c, g, st));
+  LAUNCH(run_gemv(c, g, st, &ph));
   if (top_m > 0) {
     TopmArgs ta = {};
     ta.B = B; ta.k = R - 1; ta.top_m = top_m; ta.V = m.vocab; ta.seq_ids = seq_ids; ta.drafts = tokens;
@@ -504,10 +601,16 @@ int enqueue_draft(spec_ctx* c, int B, const int32_t* seq_ids, int k, int32_t* dr
 #undef LAUNCH
 }
 
-int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st) {
+int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st, const PlaneCfg* pc) {
   g.tc_fix = c->wk.tc_fix;
   g.tc_cnt = c->wk.tc_cnt;
   g.wide = c->wk.wide;
+  if (pc) {
+    if (pc->in_xs) g.wide.xs = pc->in_xs;
+    g.wide.ready = pc->ready;
+    g.wide.out_xs = pc->out_xs;
+    g.wide.out_f16 = pc->out_f16;
+  }
   if (c->wtrace && c->wtrace_n < WTRACE_LAUNCHES) {
     unsigned long long* slot = c->wtrace + (size_t)(c->wtrace_n++) * num_sms() * 16;
     g.wide.trace = slot;  // whichever projection kernel runs records into the slot
