@@ -617,6 +617,7 @@ struct Cta {
     // the stores here or the loads below
 #pragma unroll
     for (int m = 0; m < MP; ++m) __stcg(f + m * TM + r, v[m]);
+    if (a.wide.defer) return;  // the next projection's preparation adds the partials
     epi_sync();
     if (e == 0) stamp(trace, 8);
     if (e == 0) bc[2 + (i & 1)] = (int)atomic_add_acq_rel(cnt + t, 1u);
@@ -813,9 +814,20 @@ __global__ void __launch_bounds__(Q4 ? NTHR_Q4 : NTHR, 1)
 
 // Activation rows -> bf16 (f16: fp16) hi/lo planes [2][MP][K] (gain applied) and 1/rms
 // per row (1 without a gain, 0 for the padding rows, whose planes are zero).
-__global__ void __launch_bounds__(256) wide_prep_kernel(const float* X, int ldx, int M, int K, const float* gain,
-                                                        float eps, int MP, uint16_t* xs, float* rms, int f16) {
+// Split tiles of an EPI_ADD producer that deferred them: per tile, the first
+// contributing CTA, their count and each one's partial-slot offset.
+struct FixSrc {
+  const float* fix;
+  int U, grid, C, T, MP;
+};
+constexpr int FIX_MAX_T = 128, FIX_MAX_N = 16;
+
+__global__ void __launch_bounds__(768) wide_prep_kernel(float* X, int ldx, int M, int K, const float* gain,
+                                                        float eps, int MP, uint16_t* xs, float* rms, int f16,
+                                                        FixSrc fx) {
   __shared__ float red[32];
+  __shared__ int s_n[FIX_MAX_T];
+  __shared__ int s_off[FIX_MAX_T][FIX_MAX_N];
   const int m = blockIdx.x;
   // without a gain, blocks (m, y) split the row's columns (multiples of 8)
   const int per = ((K + gridDim.y - 1) / gridDim.y + 7) / 8 * 8;
@@ -823,6 +835,21 @@ __global__ void __launch_bounds__(256) wide_prep_kernel(const float* X, int ldx,
   // The projection that follows may start at once: it fetches only weights
   // until its own wait, which also covers everything this kernel waits for.
   grid_dep_launch();
+  if (fx.fix && m < M) {
+    Plan q = {};
+    q.U = fx.U;
+    q.grid = fx.grid;
+    q.C = fx.C;
+    q.S = 1;
+    for (int t = threadIdx.x; t < fx.T; t += blockDim.x) {
+      const int bf = cta_of(t * fx.C, q), bl = cta_of(t * fx.C + fx.C - 1, q);
+      // a tile within one CTA's range was finished by that CTA
+      s_n[t] = bf == bl ? 0 : bl - bf + 1;
+      for (int bb = bf; bb <= bl && bb - bf < FIX_MAX_N; ++bb)
+        s_off[t][bb - bf] = (bb * 2 + (t == unit_begin(bb, q) / fx.C ? 0 : 1)) * fx.MP * TM;
+    }
+    __syncthreads();
+  }
   grid_dep_wait();
   uint16_t* hi = xs + (size_t)m * K;
   uint16_t* lo = xs + (size_t)(MP + m) * K;
@@ -836,8 +863,38 @@ __global__ void __launch_bounds__(256) wide_prep_kernel(const float* X, int ldx,
   }
   float ss = 0.f;
   for (int c8 = kb + threadIdx.x * 8; c8 < ke; c8 += blockDim.x * 8) {
-    const float4 u0 = __ldcg(reinterpret_cast<const float4*>(X + (size_t)m * ldx + c8));
-    const float4 u1 = __ldcg(reinterpret_cast<const float4*>(X + (size_t)m * ldx + c8 + 4));
+    float4 u0 = __ldcg(reinterpret_cast<const float4*>(X + (size_t)m * ldx + c8));
+    float4 u1 = __ldcg(reinterpret_cast<const float4*>(X + (size_t)m * ldx + c8 + 4));
+    if (fx.fix) {
+      const int t = c8 / TM, n = s_n[t];
+      if (n > 0) {
+        // the tile's partials in CTA order, then the residual: the sum the
+        // producer's last CTA would have made
+        const int r0 = c8 - t * TM;
+        float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+        for (int k0 = 0; k0 < n; k0 += 4) {
+          // four contributors' loads in flight, added in order
+          float4 p[4][2];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k0 + k < n) {
+              const float* g = fx.fix + s_off[t][k0 + k] + (size_t)m * TM + r0;
+              p[k][0] = __ldcg(reinterpret_cast<const float4*>(g));
+              p[k][1] = __ldcg(reinterpret_cast<const float4*>(g + 4));
+            }
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k0 + k < n) {
+              s0.x += p[k][0].x; s0.y += p[k][0].y; s0.z += p[k][0].z; s0.w += p[k][0].w;
+              s1.x += p[k][1].x; s1.y += p[k][1].y; s1.z += p[k][1].z; s1.w += p[k][1].w;
+            }
+        }
+        u0 = make_float4(u0.x + s0.x, u0.y + s0.y, u0.z + s0.z, u0.w + s0.w);
+        u1 = make_float4(u1.x + s1.x, u1.y + s1.y, u1.z + s1.z, u1.w + s1.w);
+        *reinterpret_cast<float4*>(X + (size_t)m * ldx + c8) = u0;
+        *reinterpret_cast<float4*>(X + (size_t)m * ldx + c8 + 4) = u1;
+      }
+    }
     float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
     if (gain) {
 #pragma unroll
@@ -1031,12 +1088,11 @@ bool gemv_wide_ok(const GemvArgs& a) {
          a.K <= a.wide.kmax && make_plan(a, num_sms(), p);
 }
 
-// M in 1..64 rows, bf16 weights, K % 64 == 0 (gemv_wide_ok). Launches the
-// activation preparation and the projection; returns 2, or -1 on an error.
-int gemv_wide(const GemvArgs& a, cudaStream_t st) {
+namespace {
+// make_plan, then the launch's cluster decision and grid
+bool final_plan(const GemvArgs& a, Plan& p) {
   std::call_once(g_once, init_encode);
-  Plan p;
-  if (!make_plan(a, num_sms(), p)) return -1;
+  if (!make_plan(a, num_sms(), p)) return false;
   while (p.S > 1 && max_clusters(p) < p.T) --p.S;
   // The cluster reduction removes the split-tile tail (about 10 us) but leaves
   // nsm - T*S SMs idle: keep it only while the streaming time those SMs would
@@ -1054,6 +1110,32 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
   } else {
     p.grid = p.T * p.S;
   }
+  return true;
+}
+}  // namespace
+
+WideSplit gemv_wide_split(const GemvArgs& a) {
+  WideSplit w = {};
+  Plan p;
+  if (!final_plan(a, p)) return w;
+  w.U = p.U;
+  w.grid = p.grid;
+  w.C = p.C;
+  w.T = p.T;
+  // CTAs on one tile: at most ceil(C / smallest range) + 1
+  const int per = p.U / p.grid;
+  const int most = per > 0 ? (p.C + per - 1) / per + 1 : p.grid;
+  w.deferrable = p.S == 1 && p.map == MAP_PLAIN && p.T <= FIX_MAX_T && most <= FIX_MAX_N;
+  return w;
+}
+
+// M in 1..64 rows, bf16 weights, K % 64 == 0 (gemv_wide_ok). Launches the
+// activation preparation (unless the planes are ready) and the projection;
+// returns the number of kernels, or -1 on an error.
+int gemv_wide(const GemvArgs& a, cudaStream_t st) {
+  Plan p;
+  if (!final_plan(a, p)) return -1;
+  if (a.wide.defer && (p.S != 1 || !gemv_wide_split(a).deferrable)) return -1;
   CUtensorMap tmw, tmx;
   const int box_rows = p.map == MAP_PAIR ? 64 : TM;
   const bool wok = p.q4 ? encode_codes(&tmw, a.W.data, a.K / 2, a.N, box_rows) : encode(&tmw, a.W.data, a.K, a.N, box_rows);
@@ -1062,15 +1144,25 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t pc = {};
-  // one block per row (the RMSNorm needs the whole row), else up to 2048
-  // columns per block
+  // one block per row (the RMSNorm needs the whole row) with a thread per 8
+  // columns (up to 768 threads), else up to 2048 columns per block of 256
   pc.gridDim = dim3(p.MP, a.gain ? 1 : (a.K + 2047) / 2048);
-  pc.blockDim = dim3(256);
+  pc.blockDim = dim3(a.gain ? std::min(768, std::max(256, (a.K / 8 + 31) / 32 * 32)) : 256);
   pc.stream = st;
   pc.attrs = attr;
   pc.numAttrs = a.pdl ? 1 : 0;
-  if (!a.wide.ready && cudaLaunchKernelEx(&pc, wide_prep_kernel, a.X, a.ldx, a.M, a.K, a.gain, a.eps, p.MP,
-                                          a.wide.xs, a.wide.rms, p.q4) != cudaSuccess)
+  FixSrc fx = {};
+  if (a.wide.fix_src) {
+    fx.fix = a.wide.fix_src;
+    fx.U = a.wide.fix_U;
+    fx.grid = a.wide.fix_grid;
+    fx.C = a.wide.fix_C;
+    fx.T = a.wide.fix_T;
+    fx.MP = p.MP;
+    if (a.wide.ready || fx.T > FIX_MAX_T || a.K != fx.T * TM) return -1;
+  }
+  if (!a.wide.ready && cudaLaunchKernelEx(&pc, wide_prep_kernel, const_cast<float*>(a.X), a.ldx, a.M, a.K,
+                                          a.gain, a.eps, p.MP, a.wide.xs, a.wide.rms, p.q4, fx) != cudaSuccess)
     return -1;
   cudaLaunchConfig_t cfg = pc;
   cfg.gridDim = dim3(p.grid);

@@ -94,6 +94,12 @@ struct WideScratch {
   // RMSNorm on it (the attention before O, the gated GELU before down):
   // `ready` = 1, no preparation kernel, 1/rms = 1.
   int ready;
+  // EPI_ADD producer: split tiles only publish their partial sums (`defer`),
+  // and the next projection's preparation adds them up, in CTA order, into the
+  // residual rows (fix_*: the producer's partials and unit split).
+  int defer;
+  const float* fix_src;
+  int fix_U, fix_grid, fix_C, fix_T;
   // This launch's EPI_GEGLU output as the next projection's planes:
   // out_xs [2][MP][N'] (N' = the output width), fp16 when out_f16 (a Q4_0
   // consumer), or null.
@@ -297,6 +303,15 @@ int gemv_tc(const GemvArgs& a, float* fix, unsigned int* cnt, cudaStream_t st);
 size_t gemv_tc_fixup_bytes();
 void setup_gemv_wide_attributes();
 bool gemv_wide_ok(const GemvArgs& a);
+// The unit split a tcgen05 launch of `a` uses (tile-major units of C 64-column
+// chunks over T tiles, balanced over `grid` CTAs), and whether its split tiles
+// can be left to the next projection's preparation (balanced ranges, at most
+// 16 CTAs on a tile, at most 128 tiles).
+struct WideSplit {
+  int U, grid, C, T;
+  bool deferrable;
+};
+WideSplit gemv_wide_split(const GemvArgs& a);
 // bf16 matrices of at least this many elements (64 MB) take the tcgen05 path at
 // any row count: they stream at about 70-90% of the HBM rate there, the
 // register-fragment kernel reaches about half of it on long rows.

@@ -221,6 +221,8 @@ struct PlaneCfg {
   int ready = 0;
   uint16_t* out_xs = nullptr;
   int out_f16 = 0;
+  int defer = 0;                 // EPI_ADD producer leaves its split tiles to the next preparation
+  WideSplit fix = {};            // consumer: the deferring producer's split (fix.U > 0: add its partials)
 };
 int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st, const PlaneCfg* pc = nullptr);
 
@@ -332,6 +334,27 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
   const int f16 = m.w_dtype == SPEC_Q4_0 ? 1 : 0;
   int rd = -1;          // buffer holding the next projection's planes
   int in_idx = 0;       // buffer the latest tcgen05 projection read
+  // A residual-add projection on the tcgen05 kernel whose consumer prepares
+  // its planes (O -> gate/up, down -> the next QKV or the LM head) leaves its
+  // split tiles' partial sums to that preparation, which adds them into the
+  // residual rows in CTA order (the sum the producer's last CTA would make):
+  // the producer's CTAs exit after their last tile instead of waiting for
+  // the arrivals and finishing tiles one by one.
+  WideSplit pending_fix = {};
+  auto defer = [&](PlaneCfg& pc, const GemvArgs& prod, bool prod_wide, bool cons_wide) {
+    if (!fuse || !prod_wide || !cons_wide || d % 128) return;
+    GemvArgs t = prod;
+    t.wide = w.wide;
+    t.tc_cnt = w.tc_cnt;
+    const WideSplit sp = gemv_wide_split(t);
+    if (!sp.deferrable) return;
+    pc.defer = 1;
+    pending_fix = sp;
+  };
+  auto fixup = [&](PlaneCfg& pc) {
+    pc.fix = pending_fix;
+    pending_fix = WideSplit{};
+  };
   auto wide_of = [&](const GemvArgs& g) {
     GemvArgs t = g;
     t.wide = w.wide;
@@ -395,6 +418,7 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     GemvArgs g = qkv_args(l);
     PlaneCfg pq;
     take(pq, wide_of(g));
+    fixup(pq);
     if (fused_rope) {
       g.epi = EPI_ROPE;
       RopeEpi& e = g.rope;
@@ -434,6 +458,7 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
 
     PlaneCfg po;
     take(po, o_wide);
+    if (m.n_experts == 0) defer(po, g, o_wide, wide_of(gu_args(l)));
     LAUNCH(run_gemv(c, g, st, &po));
 
     if (m.n_experts > 0) {
@@ -457,6 +482,7 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
     const bool gu_wide = wide_of(g);
     PlaneCfg pg;
     take(pg, gu_wide);
+    fixup(pg);
     const GemvArgs gd = down_args(l);
     const bool dn_wide = wide_of(gd);
     if (gu_wide && dn_wide) {
@@ -468,12 +494,14 @@ int enqueue_pass(spec_ctx* c, int B, const int32_t* seq_ids, int R, int mode, co
 
     PlaneCfg pd;
     take(pd, dn_wide);
+    defer(pd, gd, dn_wide, wide_of(l + 1 == m.n_layers ? head_args() : qkv_args(l + 1)));
     LAUNCH(run_gemv(c, gd, st, &pd));
   }
 
   GemvArgs g = head_args();
   PlaneCfg ph;
   take(ph, wide_of(g));
+  fixup(ph);
   TailArgs& t = g.tail;
   t.mode = mode; t.B = B; t.R = R; t.k = R - 1; t.seq_ids = seq_ids; t.drafts = tokens;
   t.out_tokens = out_tokens; t.n_emitted = n_emitted; t.seq_len = c->state.seq_len;
@@ -610,6 +638,14 @@ int run_gemv(spec_ctx* c, GemvArgs g, cudaStream_t st, const PlaneCfg* pc) {
     g.wide.ready = pc->ready;
     g.wide.out_xs = pc->out_xs;
     g.wide.out_f16 = pc->out_f16;
+    g.wide.defer = pc->defer;
+    if (pc->fix.U > 0) {
+      g.wide.fix_src = c->wk.wide.fix;
+      g.wide.fix_U = pc->fix.U;
+      g.wide.fix_grid = pc->fix.grid;
+      g.wide.fix_C = pc->fix.C;
+      g.wide.fix_T = pc->fix.T;
+    }
   }
   if (c->wtrace && c->wtrace_n < WTRACE_LAUNCHES) {
     unsigned long long* slot = c->wtrace + (size_t)(c->wtrace_n++) * num_sms() * 16;
