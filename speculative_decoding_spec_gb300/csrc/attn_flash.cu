@@ -48,6 +48,10 @@
 // skips the merge; every CTA still departs, and the last to depart resets the
 // pair's counters. Every mbarrier wait is bounded too.
 //
+// The merged rows can also be written as the O projection's bf16 (or fp16)
+// hi + lo activation planes (AttnArgs.planes), so that projection needs no
+// preparation kernel.
+//
 // The code after the last block runs once per CTA, out of a cold instruction
 // cache and at the same moment on every SM, so it is kept short: an unrolled
 // loop with per-column index divisions there cost about 8 us a launch, and a

@@ -46,6 +46,14 @@
 // of the activation rows over the cluster's CTAs in rank order (distributed
 // shared memory) and finishes those rows.
 //
+// Inside a target pass two more arrangements remove work from a launch's
+// tail. A residual-add launch whose next projection prepares its own planes
+// may leave its cut tiles to that preparation (wide.defer): the CTAs only
+// publish their partials, and the preparation adds them, in CTA order, into
+// the residual rows before it normalises them. And a gated-GELU launch may
+// write the next projection's activation planes itself (wide.out_xs), which
+// then has no preparation (wide.ready).
+//
 // Every wait is bounded: on a timeout the CTA records SPEC_ERR_TIMEOUT, stops,
 // drains its own copies and MMAs, frees its tensor memory and returns.
 #include <cuda.h>
