@@ -81,6 +81,10 @@ constexpr int CODE_BYTES = TM * KC / 2;  // 4 KB of Q4_0 codes per stage
 constexpr int W_BYTES = TM * KC * 2; // 16 KB weight tile per stage
 constexpr int XCH_LD = TM + 1;       // exchange buffer row stride (floats): conflict-free both ways
 constexpr int MAX_STAGES = 8;
+// The preparation splits every row into blocks of PREP_COLS columns; with an
+// RMSNorm each block leaves its sum of squares in rms[row][block] (at most
+// RMS_PARTS blocks) and the projection adds them in block order.
+constexpr int PREP_COLS = 1024, RMS_PARTS = 16;
 constexpr int NBARS = 3 * MAX_STAGES + 6;  // full, empty, weights-ready, 2 acc-full, 2 acc-empty, drain, pad
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr unsigned SPIN_LIMIT = 1u << 26;
@@ -666,7 +670,16 @@ struct Cta {
     if (e < 64) {
       // 1/rms of each row from the preparation kernel; planes written by the
       // producer are never normalised
-      rms_s[e] = e < a.M ? (a.wide.ready ? 1.f : __ldcg(inv_rms + e)) : 0.f;
+      float rv = 0.f;
+      if (e < a.M) {
+        rv = 1.f;
+        if (!a.wide.ready && a.gain) {
+          float tot = 0.f;
+          for (int y = 0; y < (a.K + PREP_COLS - 1) / PREP_COLS; ++y) tot += __ldcg(inv_rms + e * RMS_PARTS + y);
+          rv = rsqrtf(tot / (float)a.K + a.eps);
+        }
+      }
+      rms_s[e] = rv;
     }
     if (p.map == MAP_ROPE) load_rope_tables();
     if (a.epi == EPI_ADD) {
@@ -830,16 +843,16 @@ struct FixSrc {
 };
 constexpr int FIX_MAX_T = 128, FIX_MAX_N = 16;
 
-__global__ void __launch_bounds__(768) wide_prep_kernel(float* X, int ldx, int M, int K, const float* gain,
+__global__ void __launch_bounds__(128) wide_prep_kernel(float* X, int ldx, int M, int K, const float* gain,
                                                         float eps, int MP, uint16_t* xs, float* rms, int f16,
                                                         FixSrc fx) {
   __shared__ float red[32];
   __shared__ int s_n[FIX_MAX_T];
   __shared__ int s_off[FIX_MAX_T][FIX_MAX_N];
   const int m = blockIdx.x;
-  // without a gain, blocks (m, y) split the row's columns (multiples of 8)
-  const int per = ((K + gridDim.y - 1) / gridDim.y + 7) / 8 * 8;
-  const int kb = blockIdx.y * per, ke = min(K, kb + per);
+  // blocks (m, y) split the row's columns: a fixed split for a given K, so a
+  // row's sums do not depend on how many rows the launch has
+  const int kb = blockIdx.y * PREP_COLS, ke = min(K, kb + PREP_COLS);
   // The projection that follows may start at once: it fetches only weights
   // until its own wait, which also covers everything this kernel waits for.
   grid_dep_launch();
@@ -866,7 +879,6 @@ __global__ void __launch_bounds__(768) wide_prep_kernel(float* X, int ldx, int M
       *reinterpret_cast<uint4*>(hi + c8) = make_uint4(0, 0, 0, 0);
       *reinterpret_cast<uint4*>(lo + c8) = make_uint4(0, 0, 0, 0);
     }
-    if (threadIdx.x == 0 && blockIdx.y == 0) rms[m] = 0.f;
     return;
   }
   float ss = 0.f;
@@ -934,9 +946,7 @@ __global__ void __launch_bounds__(768) wide_prep_kernel(float* X, int ldx, int M
   }
   if (gain) {
     const float tot = block_sum(ss, red);
-    if (threadIdx.x == 0) rms[m] = rsqrtf(tot / (float)K + eps);
-  } else if (threadIdx.x == 0 && blockIdx.y == 0) {
-    rms[m] = 1.f;
+    if (threadIdx.x == 0) rms[m * RMS_PARTS + blockIdx.y] = tot;
   }
 }
 
@@ -1093,6 +1103,7 @@ size_t gemv_wide_fix_bytes() { return (size_t)num_sms() * 2 * 64 * TM * sizeof(f
 bool gemv_wide_ok(const GemvArgs& a) {
   Plan p;
   return (a.W.dtype == DT_BF16 || a.W.dtype == DT_Q4_0) && a.wide.xs && a.wide.rms && a.wide.fix && a.tc_cnt &&
+         (!a.gain || (a.K + PREP_COLS - 1) / PREP_COLS <= RMS_PARTS) &&
          a.K <= a.wide.kmax && make_plan(a, num_sms(), p);
 }
 
@@ -1152,10 +1163,9 @@ int gemv_wide(const GemvArgs& a, cudaStream_t st) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t pc = {};
-  // one block per row (the RMSNorm needs the whole row) with a thread per 8
-  // columns (up to 768 threads), else up to 2048 columns per block of 256
-  pc.gridDim = dim3(p.MP, a.gain ? 1 : (a.K + 2047) / 2048);
-  pc.blockDim = dim3(a.gain ? std::min(768, std::max(256, (a.K / 8 + 31) / 32 * 32)) : 256);
+  // PREP_COLS columns a block, a thread per 8 columns
+  pc.gridDim = dim3(p.MP, (a.K + PREP_COLS - 1) / PREP_COLS);
+  pc.blockDim = dim3(PREP_COLS / 8);
   pc.stream = st;
   pc.attrs = attr;
   pc.numAttrs = a.pdl ? 1 : 0;

@@ -85,7 +85,7 @@ struct TailArgs {
 // that path is not used and more rows run as passes of 8.
 struct WideScratch {
   uint16_t* xs;             // [2][64][kmax] bf16 activation planes (hi, lo)
-  float* rms;               // [64] 1/rms per activation row
+  float* rms;               // [64][16] per-row sums of squares of 1024-column blocks (RMSNorm)
   float* fix;               // gemv_wide_fix_bytes(): split-tile partial sums
   int kmax;                 // largest K the planes hold
   int* err;                 // device error word (timeouts), may be null

@@ -125,7 +125,7 @@ Work carve(char* base, const spec_model_desc& m, const spec_drafter_desc* d, int
     if (d) kmax = std::max({kmax, d->hidden, d->n_q_heads * m.head_dim, d->d_ff});
     w.wide.kmax = kmax;
     w.wide.xs = b.take<uint16_t>(base, gemv_wide_xs_bytes(kmax) / 2);
-    w.wide.rms = b.take<float>(base, 64);
+    w.wide.rms = b.take<float>(base, 64 * 16);  // [64 rows][16 column blocks] sums of squares
     w.wide.fix = b.take<float>(base, gemv_wide_fix_bytes() / sizeof(float));
     w.wide.err = w.err;
     w.xs_alt = b.take<uint16_t>(base, gemv_wide_xs_bytes(kmax) / 2);
@@ -891,7 +891,7 @@ size_t spec_linear_workspace_bytes(int32_t N, int32_t K, int32_t M) {
   if (N <= 0 || K <= 0 || M <= 0) return 0;
   size_t n = gemv_tc_fixup_bytes() + (((size_t)N / 8 + 64) * sizeof(unsigned int) + 255) / 256 * 256 + 256;
   if (M > 8 || ((long long)N * K >= WIDE_MIN_ELEMS && K >= WIDE_MIN_K))
-    n += gemv_wide_fix_bytes() + gemv_wide_xs_bytes(K) + 64 * sizeof(float) + 3 * 256;
+    n += gemv_wide_fix_bytes() + gemv_wide_xs_bytes(K) + 64 * 16 * sizeof(float) + 3 * 256;
   return n;
 }
 
