@@ -12,6 +12,8 @@
 // in the embedder because the final logits are the bottleneck).
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace spec {
@@ -45,7 +47,23 @@ __global__ void commit_hidden_kernel(int B, const int32_t* seq_ids, const int32_
   for (int c = threadIdx.x; c < d; c += blockDim.x) out[c] = xr[c] * inv * g[c];
 }
 
-__global__ void draft_input_kernel(DraftInArgs a) {
+// Four consecutive elements of a weight row (col % 4 == 0).
+SPEC_DEV void elem4(const Mat& W, int K, long long row, int col, float (&v)[4]) {
+  if (W.dtype == DT_F32) {
+    const float4 u = __ldg(reinterpret_cast<const float4*>((const float*)W.data + row * K + col));
+    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  } else if (W.dtype == DT_BF16) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>((const __nv_bfloat16*)W.data + row * K + col));
+    v[0] = bf16lo(u.x); v[1] = bf16hi(u.x); v[2] = bf16lo(u.y); v[3] = bf16hi(u.y);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = elem(W, K, row, col + i);
+  }
+}
+
+// [N(h); N(E[tok])] of each row (one CTA per row, four columns a thread: d %
+// 4 == 0), and the RoPE pairs of its query position.
+__global__ void __launch_bounds__(1024) draft_input_kernel(DraftInArgs a) {
   __shared__ float red[32];
   grid_dep_wait();
   grid_dep_launch();
@@ -53,17 +71,26 @@ __global__ void draft_input_kernel(DraftInArgs a) {
   const float* h = a.h_from_state ? a.h_prev + (size_t)slot * d : a.h_prev + (size_t)b * d;
   const int tok = a.j == 1 ? a.pending[slot] : a.drafts[b * a.k + a.j - 2];
   float sh = 0.f, se = 0.f;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    const float e = elem(a.embed, d, tok, c);
-    sh = fmaf(h[c], h[c], sh);
-    se = fmaf(e, e, se);
+  for (int c = 4 * threadIdx.x; c < d; c += 4 * blockDim.x) {
+    const float4 hv = __ldcg(reinterpret_cast<const float4*>(h + c));
+    float e[4];
+    elem4(a.embed, d, tok, c, e);
+    sh = fmaf(hv.x, hv.x, fmaf(hv.y, hv.y, fmaf(hv.z, hv.z, fmaf(hv.w, hv.w, sh))));
+    se = fmaf(e[0], e[0], fmaf(e[1], e[1], fmaf(e[2], e[2], fmaf(e[3], e[3], se))));
   }
   const float ih = rsqrtf(block_sum(sh, red) / (float)d + a.eps);
   const float ie = rsqrtf(block_sum(se, red) / (float)d + a.eps);
   float* cat = a.cat + (size_t)b * 2 * d;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    cat[c] = h[c] * ih * a.g_h[c];
-    cat[d + c] = elem(a.embed, d, tok, c) * ie * a.g_e[c];
+  for (int c = 4 * threadIdx.x; c < d; c += 4 * blockDim.x) {
+    const float4 hv = __ldcg(reinterpret_cast<const float4*>(h + c));
+    float e[4];
+    elem4(a.embed, d, tok, c, e);
+    const float hh[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      cat[c + i] = hh[i] * ih * a.g_h[c + i];
+      cat[d + c + i] = e[i] * ie * a.g_e[c + i];
+    }
   }
   // the drafter's query for step j sits at the position of its input token
   const int pos = a.seq_len[slot] + a.j - 1;
@@ -224,7 +251,9 @@ int commit_hidden(int B, const int32_t* seq_ids, const int32_t* sel_row, const f
 
 int draft_input(const DraftInArgs& a, cudaStream_t st) {
   cudaLaunchAttribute at[1];
-  cudaLaunchConfig_t cfg = cfg_pdl(dim3(a.B), dim3(256), 0, st, at);
+  if (a.d % 4) return -1;
+  const int threads = std::min(1024, std::max(64, (a.d / 4 + 31) / 32 * 32));
+  cudaLaunchConfig_t cfg = cfg_pdl(dim3(a.B), dim3(threads), 0, st, at);
   return cudaLaunchKernelEx(&cfg, draft_input_kernel, a) == cudaSuccess ? 1 : -1;
 }
 
