@@ -235,6 +235,18 @@ def time_dominant_kernel(tw, w, device, reps=5):
     return nbytes / len(seq), e0.elapsed_time(e1) / reps / len(seq)
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of `values` over every rank (the slowest rank's
+    times, so that the whole job's throughput is all ranks' work over it); the
+    values themselves on a single process."""
+    if not torch.distributed.is_available() or not torch.distributed.is_initialized() or \
+            torch.distributed.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
 def cpu_model():
     """The host CPU's model name (lscpu), for the baseline line."""
     try:
@@ -327,9 +339,7 @@ def run_gpu(args, w, rank, world):
     ms_total = t0.elapsed_time(t1)
     verify_ms = sum(a.elapsed_time(b) for a, b in evs) / K
     if world > 1:
-        tt = torch.tensor([ms_total, verify_ms], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_total, verify_ms = float(tt[0]), float(tt[1])
+        ms_total, verify_ms = max_over_ranks([ms_total, verify_ms], device)
         torch.distributed.barrier()
     launches = eng.kernel_launches() - launches0
     emitted, accepted = emitted_since(eng, w, stats0)
@@ -554,7 +564,13 @@ def main():
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl")
     from speculative_decoding_spec_gb300 import build
-    build.build()
+    # one rank builds the library (if it is not built yet), the others load it
+    if rank == 0:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    if rank != 0:
+        build.build()
     res, tw, eng, ctx = run_gpu(args, w, rank, world)
     eng.close()
     if rank == 0 and not args.no_cpu_baseline:
