@@ -103,32 +103,76 @@ __global__ void __launch_bounds__(1024) draft_input_kernel(DraftInArgs a) {
   }
 }
 
-// Top-C clusters of one row: bitonic sort of packed (binary32 score, id) keys,
-// larger score first, lower cluster id on ties.
-__global__ void __launch_bounds__(1024) topc_kernel(ClusterArgs a, int cpow2) {
-  extern __shared__ unsigned long long keys[];
+// Top-C clusters of one row: the top_c largest packed (binary32 score, id)
+// keys -- larger score first, lower cluster id on ties; the keys are distinct,
+// so exactly top_c keys are >= the top_c-th largest. That key is found by a
+// most-significant-digit-first radix select (8 passes of 8 bits: a shared
+// histogram of the keys that still match the prefix, then the digit where the
+// count from the top reaches the number still needed), and the keys at or
+// above it are written in any order (the member scoring does not depend on
+// it).
+__global__ void __launch_bounds__(1024) topc_kernel(ClusterArgs a, int unused) {
+  __shared__ int hist[256];
+  __shared__ unsigned long long s_prefix;
+  __shared__ int s_need, s_out;
   grid_dep_wait();
   grid_dep_launch();
-  const int b = blockIdx.x;
-  for (int i = threadIdx.x; i < cpow2; i += blockDim.x)
-    keys[i] = i < a.C ? pack_best(a.scores[(size_t)b * a.C + i], (uint32_t)i) : 0ull;
-  __syncthreads();
-  for (int k = 2; k <= cpow2; k <<= 1)
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < cpow2; i += blockDim.x) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long x = keys[i], y = keys[ixj];
-          const bool desc = (i & k) == 0;
-          if (desc ? x < y : x > y) {
-            keys[i] = y;
-            keys[ixj] = x;
+  (void)unused;
+  const int b = blockIdx.x, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    s_prefix = 0ull;
+    s_need = a.top_c;
+    s_out = 0;
+  }
+  unsigned long long mask = 0ull;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const unsigned long long prefix = s_prefix;
+    for (int i = threadIdx.x; i < a.C; i += blockDim.x) {
+      const unsigned long long key = pack_best(a.scores[(size_t)b * a.C + i], (uint32_t)i);
+      if ((key & mask) == prefix) atomicAdd(&hist[(int)((key >> shift) & 255ull)], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // lane l sums bins 255 - 8l .. 248 - 8l (from the top), then a suffix
+      // scan over the lanes finds the digit holding the need-th key
+      int c[8], tot = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        c[k] = hist[255 - 8 * lane - k];
+        tot += c[k];
+      }
+      int incl = tot;  // keys in the bins above and including this lane's
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int need = s_need, above = incl - tot;
+      if (above < need && need <= incl) {
+        int run = above;
+        for (int k = 0; k < 8; ++k) {
+          if (run + c[k] >= need) {
+            s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - k) << shift);
+            s_need = need - run;
+            break;
           }
+          run += c[k];
         }
       }
-      __syncthreads();
     }
-  for (int r = threadIdx.x; r < a.top_c; r += blockDim.x) a.chosen[b * a.top_c + r] = (int32_t)best_index(keys[r]);
+    mask |= 255ull << shift;
+    __syncthreads();
+  }
+  const unsigned long long kth = s_prefix;  // the top_c-th largest key itself
+  for (int i = threadIdx.x; i < a.C; i += blockDim.x) {
+    const unsigned long long key = pack_best(a.scores[(size_t)b * a.C + i], (uint32_t)i);
+    if (key >= kth) {
+      const int slot = atomicAdd(&s_out, 1);
+      if (slot < a.top_c) a.chosen[b * a.top_c + slot] = i;
+    }
+  }
 }
 
 // Score the member rows of one chosen cluster; the best (score, token id) of a
@@ -257,16 +301,13 @@ int draft_input(const DraftInArgs& a, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, draft_input_kernel, a) == cudaSuccess ? 1 : -1;
 }
 
-void setup_draft_attributes() {
-  cudaFuncSetAttribute(topc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-}
+void setup_draft_attributes() {}
 
 int cluster_head(const ClusterArgs& a, cudaStream_t st) {
-  int cp = 1;
-  while (cp < a.C) cp <<= 1;
+  if (a.top_c < 1 || a.top_c > a.C) return -1;
   cudaLaunchAttribute at[1];
-  cudaLaunchConfig_t cfg = cfg_pdl(dim3(a.B), dim3(1024), (size_t)cp * 8, st, at);
-  if (cudaLaunchKernelEx(&cfg, topc_kernel, a, cp) != cudaSuccess) return -1;
+  cudaLaunchConfig_t cfg = cfg_pdl(dim3(a.B), dim3(1024), 0, st, at);
+  if (cudaLaunchKernelEx(&cfg, topc_kernel, a, 0) != cudaSuccess) return -1;
   cudaLaunchConfig_t cfg2 = cfg_pdl(dim3(a.B, a.top_c), dim3(256), (size_t)a.h * 4, st, at);
   if (cudaLaunchKernelEx(&cfg2, members_kernel, a) != cudaSuccess) return -1;
   return 2;
